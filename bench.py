@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark: one decode step of paged attention per iteration, on GB300.
+
+A step is the whole hot path over one batch: pa_reshape_and_cache writes each
+sequence's newest token into its slot, then pa_decode attends over every
+sequence (the serving order: the new token's K/V is in the cache before the
+attention kernel runs). Default workload: Llama-3-8B-shaped GQA decode
+(128 sequences, 32 query / 8 kv heads, head_dim 128, block size 16, lengths
+uniform in [1024, 8192], bf16, random block placement, seed 0).
+
+Prints one JSON line. ``value`` is effective GB/s: the algorithmic bytes of the
+step (K/V rows of every valid token, table entries, lengths, q and out, plus
+the cache write's reads and writes) divided by device time, with inputs
+resident in HBM. Per step ~2.4 GB of K/V is read, far more than the 129 MB
+L2, so no L2 flush is needed between steps.
+
+``--impl reference`` times the float64 CPU oracle instead (on a bounded
+sample of the same workload) and prints the same metric.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(seed = rank): weak scaling, no data-path collective; the timing is the max
+over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+# the CPU oracle leg is timed single-threaded; say so instead of guessing BLAS threads
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention: effective KV-read GB/s (% of HBM peak), tokens/s"
+DEFAULT_WORKLOAD = "llama3_8b_gqa"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _traffic(workload: str):
+    """DRAM bytes per decode launch from a committed ncu capture, if the kernel is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(workload)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "paged_kv_cache_305_gb300", "csrc", "decode.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("source_sha256"):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        busy = [x for x in sm if smax and x > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg
+# ---------------------------------------------------------------------------
+def _pair_bytes(case, s):
+    """Algorithmic bytes attributed to one (sequence, query head) of the decode."""
+    L, B = int(case.seq_lens[s]), case.block_size
+    seq = 2 * L * case.num_kv_heads * case.head_dim * 2 + 4 * ((L + B - 1) // B) + 4
+    return seq / case.num_q_heads + 2 * case.head_dim * 2
+
+
+def oracle_prepare(case):
+    """The step's cache write, applied by the oracle to the host caches (in place)."""
+    import oracle
+    oracle.reshape_and_cache(case.new_key, case.new_value, case.key_cache, case.value_cache,
+                             case.slot_mapping, case.block_size, in_place=True)
+
+
+def time_oracle(case, budget_s: float, start: int = 0):
+    """Run the float64 oracle over (sequence, query head) output rows of the batch,
+    from row ``start`` on (wrapping), until ``budget_s`` is spent (at least one row).
+
+    Returns (GB/s over the rows' share of the algorithmic bytes, seconds, rows done).
+    """
+    import oracle
+    S, Hq = case.num_seqs, case.num_q_heads
+    t0 = time.perf_counter()
+    done, nbytes = 0, 0.0
+    while True:
+        i = (start + done) % (S * Hq)
+        s, hq = i // Hq, i % Hq
+        oracle.paged_decode_pairs(case.query, case.key_cache, case.value_cache, case.block_tables,
+                                  case.seq_lens, case.block_size, case.scale, case.dtype, [(s, hq)])
+        nbytes += _pair_bytes(case, s)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s or done >= S * Hq:
+            break
+    dt = time.perf_counter() - t0
+    return nbytes / dt / 1e9, dt, done
+
+
+def cpu_baseline_block(case, budget_s):
+    t0 = time.perf_counter()
+    oracle_prepare(case)
+    gbs, dt, done = time_oracle(case, budget_s)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"float64 NumPy oracle (one thread): {done} of {case.num_seqs * case.num_q_heads} "
+                      f"(sequence, query head) output rows of the same batch in {dt:.1f} s "
+                      f"(after its cache write, {time.perf_counter() - t0 - dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    case = W.make_workload(args.workload, seed=0, block_size=args.block_size)
+    oracle_prepare(case)
+    # every step is a bounded sample, sized so that warm-up + steps take ~2 minutes
+    per_step = max(0.002, min(args.ref_budget, 120.0 / max(1, args.steps + args.warmup)))
+    pos = 0
+    for _ in range(args.warmup):
+        _, _, n = time_oracle(case, per_step, pos)
+        pos += n
+    tot_bytes, tot_s, rows = 0.0, 0.0, 0
+    for _ in range(args.steps):
+        gbs, dt, n = time_oracle(case, per_step, pos)
+        pos += n
+        rows += n
+        tot_bytes += gbs * dt * 1e9
+        tot_s += dt
+    gbs = tot_bytes / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
+        "data": "synthetic", "config": _config(case, args),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"float64 NumPy oracle (one thread): {rows} (sequence, query head) "
+                                   f"output rows over {args.steps} steps of ~{per_step:.3f} s each"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(case, args):
+    return {"workload": case.name, "num_seqs": case.num_seqs, "num_q_heads": case.num_q_heads,
+            "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
+            "block_size": case.block_size, "seq_len_range": [int(case.seq_lens.min()),
+                                                             int(case.seq_lens.max())],
+            "mean_seq_len": round(float(case.seq_lens.mean()), 1),
+            "partition_tokens": args.partition_tokens or 512,
+            "kv_bytes_per_step": case.kv_bytes(),
+            "l2": "no flush: inputs larger than L2 (KV read per step >> 129 MB)",
+            "parallelism": "replicas (weak scaling, no collective)", "seed": 0}
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+
+    pbuild.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    case = W.make_workload(args.workload, seed=rank,
+                           block_size=args.block_size if args.workload == "shared_prefix" else None)
+    pt = args.partition_tokens if args.partition_tokens is not None else case.partition_tokens
+    tdt = {"fp16": torch.float16, "bf16": torch.bfloat16}[case.dtype]
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(tdt)
+
+    q, kc, vc = up(case.query), up(case.key_cache), up(case.value_cache)
+    nk, nv = up(case.new_key), up(case.new_value)
+    bt = torch.from_numpy(case.block_tables).to(dev)
+    sl = torch.from_numpy(case.seq_lens).to(dev)
+    slots = torch.from_numpy(case.slot_mapping).to(dev)
+    out = torch.empty_like(q)
+    ws = pa.alloc_workspace(q, kc, bt, pt)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pa.reshape_and_cache(nk, nv, kc, vc, slots)
+        pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    dec_bytes = case.algorithmic_bytes()
+    step_bytes = dec_bytes + case.cache_write_bytes()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                      int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
+        start.record(stream)
+        for i in range(K):
+            pa.reshape_and_cache(nk, nv, kc, vc, slots)
+            ev[i][0].record(stream)
+            pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms = start.elapsed_time(stop)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # end to end through the public API: pinned host inputs in, result out, every step
+    h = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16) if v.dtype == np.uint16 else v)
+         .pin_memory() for k, v in (("q", case.query), ("nk", case.new_key), ("nv", case.new_value),
+                                    ("bt", case.block_tables), ("sl", case.seq_lens),
+                                    ("slots", case.slot_mapping))}
+    host_out = torch.empty(out.shape, dtype=torch.int16).pin_memory()
+    d_in = {"q": q.view(torch.int16), "nk": nk.view(torch.int16), "nv": nv.view(torch.int16),
+            "bt": bt, "sl": sl, "slots": slots}
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for k in h:
+            d_in[k].copy_(h[k], non_blocking=True)
+        step()
+        host_out.copy_(out.view(torch.int16), non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    Ke = min(K, args.e2e_steps)
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    if dist is not None:
+        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    peak, peak_kind = _peaks()
+    dec_mean_ms = statistics.mean(dec_ms)
+    achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
+    value = step_bytes * K * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms / K, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
+        "data": "synthetic", "config": _config(case, args) | {"partition_tokens": pt or 512},
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "tokens_per_s": round(case.num_seqs * K * world / (ms * 1e-3), 1),
+        "kv_tokens_per_s": round(float(case.seq_lens.sum()) * K * world / (ms * 1e-3), 1),
+        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
+                     "algorithmic_bytes": dec_bytes,
+                     "mean_launch_us": round(dec_mean_ms * 1e3, 2),
+                     "median_launch_us": round(statistics.median(dec_ms) * 1e3, 2)},
+        "e2e": {"value": round(step_bytes * Ke * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
+        "gpu_launches": 2 * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_block(W.make_workload(args.workload, seed=0,
+                                                  block_size=args.block_size), args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(W.WORKLOADS) + ["shared_prefix"])
+    ap.add_argument("--block-size", type=int, default=16, help="shared_prefix only")
+    ap.add_argument("--partition-tokens", type=int, default=None)
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

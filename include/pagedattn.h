@@ -1,0 +1,154 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn.so: paged KV-cache decode attention
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is single-query decode attention over a KV cache kept in
+ * fixed-size physical blocks that a per-sequence block table addresses
+ * ("Paged Attention > The PagedAttention Algorithm", Standard Attention vs
+ * PagedAttention: softmax(q K^T / sqrt(d_k)) V, with K and V gathered through
+ * the block table; "PagedAttention by hand", Forward pass, Steps 2-4). The
+ * result equals standard attention over the sequence's tokens in logical
+ * order.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is DEVICE memory owned by the caller, unless the
+ *     parameter says otherwise. The library allocates nothing and keeps no
+ *     state except a thread-local error string and one device-resident counter
+ *     of rejected indices (see pa_bad_index_count).
+ *   - Work is enqueued on `stream` and returns without synchronising. Inputs
+ *     must stay valid until the stream reaches the work.
+ *   - A negative return value means the call enqueued nothing (or, for
+ *     PA_ERR_CUDA, that a launch failed); pa_last_error() then describes it.
+ *   - 16-bit elements are IEEE fp16 or bfloat16 (`pa_dtype`), row-major.
+ *   - Every tensor pointer must be 16-byte aligned.
+ *
+ * Layouts (S = num_seqs, Hq / Hkv = query / kv heads, d = head_dim,
+ * B = block_size, NB = num_blocks, MB = max_blocks_per_seq):
+ *   query, out          [S, Hq, d]
+ *   key_cache,
+ *   value_cache         [NB, B, Hkv, d]   (the physical block pool)
+ *   block_tables        [S, MB] int32     (physical block ids)
+ *   seq_lens            [S] int32
+ *   key, value (new)    [T, Hkv, d]
+ *   slot_mapping        [T] int64         (physical block * B + offset)
+ * Query head hq reads kv head hq / (Hq / Hkv) (contiguous groups).
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_FLOAT16 = 0, PA_BFLOAT16 = 1 } pa_dtype;
+
+enum {
+  PA_OK = 0,
+  PA_ERR_INVALID = -1,     /* a null pointer, a bad size or a misaligned pointer */
+  PA_ERR_UNSUPPORTED = -2, /* valid, but outside what the kernels are built for */
+  PA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
+  PA_ERR_CUDA = -4         /* a CUDA call failed; the message names it */
+};
+
+/*
+ * Cache write: for every token i < num_tokens with slot = slot_mapping[i] >= 0,
+ * copy the rows key[i, :, :] and value[i, :, :] ([Hkv, d] each) into
+ * key_cache[slot / B, slot % B, :, :] and value_cache[...] bit for bit.
+ * A negative slot skips token i. This is the write vLLM performs for the new
+ * token before the attention kernel runs ("PagedAttention by hand", Setup,
+ * Step 1; Code: "fused reshape and block write"); the slot of logical token t
+ * of a sequence is table[t / B] * B + t % B ("The PagedAttention Algorithm":
+ * logical token to "slot 9 in block 47").
+ *
+ * Sizes: num_tokens >= 0 (0 is a no-op), num_kv_heads >= 1, head_dim in
+ * {64, 128}, block_size a power of two in [1, 64], num_blocks >= 1.
+ * A slot >= num_blocks * block_size is not written and is counted by
+ * pa_bad_index_count. Two tokens with the same slot race (one of them wins).
+ * Errors: PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA.
+ */
+int pa_reshape_and_cache(const void* key, const void* value,
+                         void* key_cache, void* value_cache,
+                         const int64_t* slot_mapping, int num_tokens,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * Workspace bytes pa_decode needs for these sizes (0 when one partition
+ * covers the longest possible sequence, max_blocks_per_seq * block_size).
+ * partition_tokens is the value that will be passed to pa_decode (0 = the
+ * library's default, 512 tokens). Returns 0 for invalid sizes.
+ *
+ * Workspace contents: per-(sequence, kv-head) arrival counters followed by
+ * fp32 partial results. The counters must be ZERO before the first pa_decode
+ * that uses a workspace; every pa_decode leaves them zero again when it
+ * completes, so one zero-fill at allocation is enough. Calls that share a
+ * workspace must not overlap on the GPU.
+ */
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size,
+                                 int partition_tokens);
+
+/*
+ * Decode attention. For every sequence s and query head hq, with
+ * h = hq / (Hq / Hkv) and L = seq_lens[s]:
+ *   score_t = scale * <query[s, hq, :], K_t>,        t = 0 .. L-1
+ *   out[s, hq, :] = sum_t softmax(score)_t * V_t
+ * where K_t / V_t = key_cache / value_cache[block_tables[s, t / B], t % B, h, :].
+ * Slots at or past L and table entries at or past ceil(L / B) are never read.
+ * L = 0 gives a zero output row. The output is rounded to `dtype` (nearest
+ * even); arithmetic is fp32 with 16-bit (dtype) products.
+ *
+ * The first twelve parameters follow the statement of the problem; the rest
+ * give the table's row stride (max_blocks_per_seq), the pool size for index
+ * checks (num_blocks), the split-K partition length, the element type, the
+ * scratch space and the stream.
+ *
+ * Split-K: each sequence is cut into partitions of partition_tokens tokens
+ * (0 = default 512; otherwise a multiple of 16 and of block_size, at most
+ * 16384, and at most 4096 table entries long). Each partition's result is
+ * combined by log-sum-exp inside the same kernel launch, so the call is a
+ * single kernel. `workspace` must hold pa_decode_workspace_bytes(...) bytes
+ * (it may be NULL when that is 0); see there for the zeroing rule.
+ *
+ * Sizes: num_seqs >= 0 (0 is a no-op) and <= 65535, num_kv_heads in
+ * [1, 65535], num_q_heads a multiple of num_kv_heads with at most 16 query
+ * heads per kv head, head_dim in {64, 128}, block_size a power of two in
+ * [1, 64], max_blocks_per_seq >= 1, num_blocks >= 1, scale finite.
+ * A seq_len above max_blocks_per_seq * block_size is clamped to it, and a
+ * block id outside [0, num_blocks) reads as zeros; both are counted by
+ * pa_bad_index_count and never fault.
+ * Errors: PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA.
+ */
+int pa_decode(void* out, const void* query,
+              const void* key_cache, const void* value_cache,
+              const int32_t* block_tables, const int32_t* seq_lens,
+              int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+              int block_size, float scale,
+              int max_blocks_per_seq, int num_blocks, int partition_tokens,
+              pa_dtype dtype, void* workspace, size_t workspace_bytes,
+              cudaStream_t stream);
+
+/*
+ * Message for the most recent non-OK return on the calling thread ("" if
+ * none). The pointer stays valid until the next library call on that thread.
+ */
+const char* pa_last_error(void);
+
+/*
+ * Number of out-of-range indices (block ids, slots, sequence lengths) the
+ * kernels on the CURRENT device have skipped or clamped since the counter was
+ * last cleared. Synchronises the device. Writes the count to *count (a host
+ * pointer); clears the counter when `clear` is non-zero.
+ * Errors: PA_ERR_INVALID (count is NULL), PA_ERR_CUDA.
+ */
+int pa_bad_index_count(unsigned long long* count, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

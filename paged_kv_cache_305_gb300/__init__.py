@@ -1,0 +1,17 @@
+"""Paged KV-cache decode attention for GB300 (sm_103a).
+
+The computation lives in ``libpagedattn.so`` (C ABI in ``include/pagedattn.h``);
+``pagedattn`` is its Python binding.
+"""
+from .pagedattn import (  # noqa: F401
+    PA_BFLOAT16,
+    PA_FLOAT16,
+    PagedAttnError,
+    alloc_workspace,
+    bad_index_count,
+    decode,
+    decode_workspace_bytes,
+    last_error,
+    load_library,
+    reshape_and_cache,
+)

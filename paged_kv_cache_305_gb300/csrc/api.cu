@@ -1,0 +1,253 @@
+// C-ABI layer of libpagedattn.so: argument checks, workspace carve-up,
+// dispatch to the kernels, and error reporting. Declarations and the
+// contract of every entry point are in include/pagedattn.h.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <atomic>
+#include <string>
+
+#include "internal.h"
+#include "pagedattn.h"
+
+namespace {
+
+thread_local std::string g_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+int log2_pow2(int b) {  // -1 unless b is a power of two in [1, 64]
+  for (int k = 0; k <= 6; ++k)
+    if (b == (1 << k)) return k;
+  return -1;
+}
+
+// Device-resident counter of out-of-range indices the kernels skipped.
+__device__ unsigned long long g_bad_index_count;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned long long*> g_bad_ptr[kMaxDevices];
+
+int bad_counter(unsigned long long** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index %d", dev);
+  unsigned long long* p = g_bad_ptr[dev].load(std::memory_order_acquire);
+  if (p == nullptr) {
+    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_bad_index_count);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(bad-index counter)");
+    g_bad_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return PA_OK;
+}
+
+int check_dtype(pa_dtype dtype) {
+  if (dtype != PA_FLOAT16 && dtype != PA_BFLOAT16)
+    return fail(PA_ERR_INVALID, "dtype %d is neither PA_FLOAT16 nor PA_BFLOAT16", (int)dtype);
+  return PA_OK;
+}
+
+int resolve_partition(int partition_tokens, int block_size, int* pt) {
+  int p = partition_tokens == 0 ? pa::kDefaultPartitionTokens : partition_tokens;
+  if (p < 0) return fail(PA_ERR_INVALID, "partition_tokens %d < 0", partition_tokens);
+  if (p % 16 != 0 || p % block_size != 0)
+    return fail(PA_ERR_INVALID, "partition_tokens %d must be a multiple of 16 and of block_size %d",
+                p, block_size);
+  if (p > pa::kMaxPartitionTokens)
+    return fail(PA_ERR_UNSUPPORTED, "partition_tokens %d > %d", p, pa::kMaxPartitionTokens);
+  if (p / block_size > pa::kMaxTableEntriesPerPartition)
+    return fail(PA_ERR_UNSUPPORTED, "a partition spans %d table entries (> %d)", p / block_size,
+                pa::kMaxTableEntriesPerPartition);
+  *pt = p;
+  return PA_OK;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+namespace pa {
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions) {
+  WorkspaceLayout w{};
+  const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
+  if (max_partitions <= 1) return w;
+  w.count_off = 0;
+  w.lse_off = round_up(rows * sizeof(int), 256);
+  w.out_off = w.lse_off + round_up(rows * max_partitions * sizeof(float), 256);
+  w.total = w.out_off + rows * max_partitions * static_cast<size_t>(head_dim) * sizeof(float);
+  return w;
+}
+}  // namespace pa
+
+extern "C" {
+
+const char* pa_last_error(void) { return g_error.c_str(); }
+
+int pa_bad_index_count(unsigned long long* count, int clear) {
+  g_error.clear();
+  if (count == nullptr) return fail(PA_ERR_INVALID, "count is NULL");
+  unsigned long long* p = nullptr;
+  int rc = bad_counter(&p);
+  if (rc != PA_OK) return rc;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(count, p, sizeof(*count), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(bad-index counter)");
+  if (clear) {
+    e = cudaMemset(p, 0, sizeof(*p));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(bad-index counter)");
+  }
+  return PA_OK;
+}
+
+int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         cudaStream_t stream) {
+  g_error.clear();
+  int rc = check_dtype(dtype);
+  if (rc != PA_OK) return rc;
+  if (num_tokens < 0) return fail(PA_ERR_INVALID, "num_tokens %d < 0", num_tokens);
+  if (num_kv_heads < 1) return fail(PA_ERR_INVALID, "num_kv_heads %d < 1", num_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (log2_pow2(block_size) < 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two up to 64)", block_size);
+  if (num_blocks < 1) return fail(PA_ERR_INVALID, "num_blocks %d < 1", num_blocks);
+  if (num_tokens == 0) return PA_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+    return fail(PA_ERR_INVALID, "a pointer argument is NULL");
+  if (!aligned16(key) || !aligned16(value) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID, "key, value and the caches must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(slot_mapping) & 7u) != 0)
+    return fail(PA_ERR_INVALID, "slot_mapping must be 8-byte aligned");
+  const long long row_bytes = static_cast<long long>(num_kv_heads) * head_dim * 2;
+  if (row_bytes > (1ll << 30)) return fail(PA_ERR_UNSUPPORTED, "a token row of %lld bytes", row_bytes);
+  unsigned long long* bad = nullptr;
+  rc = bad_counter(&bad);
+  if (rc != PA_OK) return rc;
+  cudaError_t e = pa::launch_reshape_and_cache(
+      key, value, key_cache, value_cache, slot_mapping, num_tokens, static_cast<int>(row_bytes),
+      static_cast<long long>(num_blocks) * block_size, bad, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return PA_OK;
+}
+
+size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_blocks_per_seq, int block_size, int partition_tokens) {
+  if (num_seqs < 0 || num_q_heads < 1 || (head_dim != 64 && head_dim != 128) ||
+      max_blocks_per_seq < 1 || log2_pow2(block_size) < 0)
+    return 0;
+  int pt = 0;
+  std::string saved = g_error;
+  if (resolve_partition(partition_tokens, block_size, &pt) != PA_OK) {
+    g_error = saved;
+    return 0;
+  }
+  const long long lmax = static_cast<long long>(max_blocks_per_seq) * block_size;
+  const long long parts = (lmax + pt - 1) / pt;
+  return pa::workspace_layout(num_seqs, num_q_heads, head_dim, static_cast<int>(parts)).total;
+}
+
+int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+              int max_blocks_per_seq, int num_blocks, int partition_tokens, pa_dtype dtype,
+              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_error.clear();
+  int rc = check_dtype(dtype);
+  if (rc != PA_OK) return rc;
+  if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+  if (num_q_heads < 1 || num_kv_heads < 1)
+    return fail(PA_ERR_INVALID, "num_q_heads %d / num_kv_heads %d must be >= 1", num_q_heads,
+                num_kv_heads);
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  if (group > pa::kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "%d query heads per kv head (> %d)", group, pa::kMaxGroup);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  const int shift = log2_pow2(block_size);
+  if (shift < 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two up to 64)", block_size);
+  if (max_blocks_per_seq < 1) return fail(PA_ERR_INVALID, "max_blocks_per_seq %d < 1", max_blocks_per_seq);
+  if (num_blocks < 1) return fail(PA_ERR_INVALID, "num_blocks %d < 1", num_blocks);
+  if (!isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
+  int pt = 0;
+  rc = resolve_partition(partition_tokens, block_size, &pt);
+  if (rc != PA_OK) return rc;
+  const long long lmax = static_cast<long long>(max_blocks_per_seq) * block_size;
+  if (lmax > 0x7fffffffll)
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size = %lld overflows int", lmax);
+  if (num_seqs > 65535 || num_kv_heads > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "num_seqs %d / num_kv_heads %d above 65535", num_seqs,
+                num_kv_heads);
+  if (num_seqs == 0) return PA_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens)
+    return fail(PA_ERR_INVALID, "a pointer argument is NULL");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID, "out, query and the caches must be 16-byte aligned");
+  if (!aligned4(block_tables) || !aligned4(seq_lens))
+    return fail(PA_ERR_INVALID, "block_tables and seq_lens must be 4-byte aligned");
+
+  const int parts = static_cast<int>((lmax + pt - 1) / pt);
+  const pa::WorkspaceLayout wl = pa::workspace_layout(num_seqs, num_q_heads, head_dim, parts);
+  if (wl.total > 0) {
+    if (workspace == nullptr || workspace_bytes < wl.total)
+      return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", wl.total,
+                  workspace == nullptr ? (size_t)0 : workspace_bytes);
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+  }
+  unsigned long long* bad = nullptr;
+  rc = bad_counter(&bad);
+  if (rc != PA_OK) return rc;
+
+  pa::DecodeArgs a{};
+  a.out = out;
+  a.query = query;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  a.block_shift = shift;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.partition_tokens = pt;
+  a.max_partitions = parts;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  char* ws = static_cast<char*>(workspace);
+  a.ws_count = wl.total ? reinterpret_cast<int*>(ws + wl.count_off) : nullptr;
+  a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
+  a.ws_out = wl.total ? reinterpret_cast<float*>(ws + wl.out_off) : nullptr;
+  a.bad = bad;
+  cudaError_t e = pa::launch_decode(a, head_dim, dtype == PA_BFLOAT16, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime_api.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace pa {
+
+constexpr int kDefaultPartitionTokens = 512;
+constexpr int kMaxPartitionTokens = 16384;
+constexpr int kMaxTableEntriesPerPartition = 4096;
+constexpr int kMaxGroup = 16;  // query heads per kv head (rows of one mma tile)
+
+struct DecodeArgs {
+  void* out;
+  const void* query;
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;          // num_q_heads / num_kv_heads
+  int block_shift;    // log2(block_size)
+  int max_blocks_per_seq;
+  int num_blocks;
+  int partition_tokens;
+  int max_partitions;  // ceil(max_blocks_per_seq * block_size / partition_tokens)
+  float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+  float* ws_out;       // [S, Hq, max_partitions, d] fp32 partial outputs (normalised)
+  float* ws_lse;       // [S, Hq, max_partitions] fp32 base-2 log-sum-exp
+  int* ws_count;       // [S * Hkv] arrival counters (zero between calls)
+  unsigned long long* bad;  // device counter of rejected indices
+};
+
+// Workspace carve-up shared by pa_decode_workspace_bytes and pa_decode.
+struct WorkspaceLayout {
+  size_t count_off, lse_off, out_off, total;
+};
+WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions);
+
+// Launchers: return a cudaError_t from the launch (cudaSuccess on success).
+cudaError_t launch_decode(const DecodeArgs& a, int head_dim, bool bf16, cudaStream_t stream);
+size_t decode_smem_bytes(int head_dim, int table_entries);
+
+cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
+                                     void* value_cache, const int64_t* slot_mapping,
+                                     int num_tokens, int row_bytes, long long num_slots,
+                                     unsigned long long* bad, cudaStream_t stream);
+
+}  // namespace pa

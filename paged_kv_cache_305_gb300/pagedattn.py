@@ -1,0 +1,165 @@
+"""Python binding of libpagedattn.so (ctypes; argument marshalling only).
+
+Every step of the computation runs in the library's CUDA kernels. PyTorch is
+used for device memory and streams only: tensors are passed by
+``data_ptr()`` and work is enqueued on the current CUDA stream of the
+tensors' device. If the library is missing this module raises; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedattn.so")
+
+PA_FLOAT16, PA_BFLOAT16 = 0, 1
+_DTYPES = {torch.float16: PA_FLOAT16, torch.bfloat16: PA_BFLOAT16}
+EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
+            "pa_last_error", "pa_bad_index_count")
+
+_lib = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"pagedattn error {code}: {msg}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libpagedattn.so and declare the C signatures (raises if absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is not built: run `python -m paged_kv_cache_305_gb300.build` "
+            "(needs nvcc); there is no CPU fallback")
+    L = ctypes.CDLL(path)
+    vp, i32, i64p, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    L.pa_reshape_and_cache.argtypes = [vp, vp, vp, vp, i64p, i32, i32, i32, i32, i32, i32, vp]
+    L.pa_reshape_and_cache.restype = i32
+    L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.pa_decode_workspace_bytes.restype = sz
+    L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
+                            i32, i32, i32, i32, vp, sz, vp]
+    L.pa_decode.restype = i32
+    L.pa_last_error.argtypes = []
+    L.pa_last_error.restype = ctypes.c_char_p
+    L.pa_bad_index_count.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
+    L.pa_bad_index_count.restype = i32
+    _lib = L
+    return L
+
+
+def last_error() -> str:
+    return load_library().pa_last_error().decode()
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise PagedAttnError(rc, last_error())
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype} (float16 or bfloat16)")
+    return _DTYPES[t.dtype]
+
+
+def _need(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                      value_cache: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """Write key/value [T, Hkv, d] rows into the caches [NB, B, Hkv, d] at slot_mapping [T] (int64)."""
+    _need(key.is_cuda and key.is_contiguous() and value.is_contiguous()
+          and key_cache.is_contiguous() and value_cache.is_contiguous()
+          and slot_mapping.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    _need(slot_mapping.dtype == torch.int64, "slot_mapping must be int64")
+    _need(key.dtype == value.dtype == key_cache.dtype == value_cache.dtype, "dtype mismatch")
+    NB, B, Hkv, d = key_cache.shape
+    _need(value_cache.shape == key_cache.shape, "key/value cache shape mismatch")
+    T = key.shape[0]
+    _need(key.shape == (T, Hkv, d) and value.shape == (T, Hkv, d), "key/value shape mismatch")
+    _need(slot_mapping.shape == (T,), "slot_mapping shape mismatch")
+    L = load_library()
+    with torch.cuda.device(key.device):
+        _check(L.pa_reshape_and_cache(key.data_ptr(), value.data_ptr(), key_cache.data_ptr(),
+                                      value_cache.data_ptr(), slot_mapping.data_ptr(), T, Hkv, d,
+                                      B, NB, _dtype_code(key), _stream(key, stream)))
+
+
+def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
+                           max_blocks_per_seq: int, block_size: int,
+                           partition_tokens: int = 0) -> int:
+    return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
+                                                        max_blocks_per_seq, block_size,
+                                                        partition_tokens))
+
+
+def alloc_workspace(query: torch.Tensor, key_cache: torch.Tensor, block_tables: torch.Tensor,
+                    partition_tokens: int = 0) -> Optional[torch.Tensor]:
+    """Zero-filled workspace for :func:`decode` with these shapes (None if none is needed)."""
+    S, Hq, d = query.shape
+    n = decode_workspace_bytes(S, Hq, d, block_tables.shape[1], key_cache.shape[1], partition_tokens)
+    if n == 0:
+        return None
+    return torch.zeros(n, dtype=torch.uint8, device=query.device)
+
+
+def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+           value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+           scale: Optional[float] = None, partition_tokens: int = 0,
+           workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Paged decode attention into ``out`` [S, Hq, d]; returns ``out``.
+
+    ``query`` [S, Hq, d]; caches [NB, B, Hkv, d]; ``block_tables`` [S, MB]
+    int32; ``seq_lens`` [S] int32. ``scale`` defaults to 1/sqrt(d). The
+    workspace, when one is needed, comes from :func:`alloc_workspace` (zeroed
+    once, reusable across calls on one stream).
+    """
+    S, Hq, d = query.shape
+    NB, B, Hkv, d2 = key_cache.shape
+    _need(d2 == d and value_cache.shape == key_cache.shape, "cache shape mismatch")
+    _need(out.shape == query.shape and out.dtype == query.dtype == key_cache.dtype == value_cache.dtype,
+          "out/query/cache dtype or shape mismatch")
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S and seq_lens.shape == (S,),
+          "block_tables/seq_lens shape mismatch")
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    L = load_library()
+    with torch.cuda.device(query.device):
+        _check(L.pa_decode(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
+                           value_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(),
+                           S, Hq, Hkv, d, B, float(scale), block_tables.shape[1], NB,
+                           partition_tokens, _dtype_code(query), ws_ptr, ws_bytes,
+                           _stream(query, stream)))
+    return out
+
+
+def bad_index_count(clear: bool = False) -> int:
+    """Out-of-range indices the kernels skipped on the current device (synchronises)."""
+    n = ctypes.c_ulonglong(0)
+    _check(load_library().pa_bad_index_count(ctypes.byref(n), int(bool(clear))))
+    return int(n.value)

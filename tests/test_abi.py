@@ -1,0 +1,141 @@
+"""The C-ABI library builds, loads and exports what include/pagedattn.h declares;
+its host-side argument checks reject bad calls before touching the GPU.
+
+Nothing here launches a kernel, so it runs without a GPU.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_305_gb300 as pa
+from paged_kv_cache_305_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(pa_\w+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    pbuild.build()
+    return pa.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"pa_decode", "pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pa.pagedattn.EXPORTED) <= set(names)
+
+
+def test_library_is_built_for_sm_103a_only():
+    assert pbuild.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_workspace_bytes_arithmetic(lib):
+    # S * Hq counters, then S * Hq * P lse values, then S * Hq * P * d outputs (fp32)
+    def expect(S, Hq, d, MB, B, pt):
+        P = -(-(MB * B) // (pt or 512))
+        if P <= 1:
+            return 0
+        r = lambda x: -(-x // 256) * 256
+        rows = S * Hq
+        return r(rows * 4) + r(rows * P * 4) + rows * P * d * 4
+    for args in [(128, 32, 128, 512, 16, 0), (8, 64, 128, 8192, 16, 512), (4, 4, 64, 8, 16, 0),
+                 (3, 6, 64, 40, 1, 16), (256, 32, 128, 24, 64, 64)]:
+        assert pa.decode_workspace_bytes(*args) == expect(*args), args
+    # invalid sizes give 0
+    assert pa.decode_workspace_bytes(4, 4, 96, 8, 16, 0) == 0
+    assert pa.decode_workspace_bytes(4, 4, 64, 8, 3, 0) == 0
+    assert pa.decode_workspace_bytes(4, 4, 64, 8, 16, 24) == 0
+
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced by these calls
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, S=2, Hq=8, Hkv=2, d=128,
+             B=16, scale=0.1, MB=4, NB=100, pt=0, dtype=1, ws=None, wsb=0)
+    a.update(kw)
+    return lib.pa_decode(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["sl"], a["S"], a["Hq"],
+                         a["Hkv"], a["d"], a["B"], a["scale"], a["MB"], a["NB"], a["pt"], a["dtype"],
+                         a["ws"], a["wsb"], None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dtype=5), -1, "dtype"),
+    (dict(S=-1), -1, "num_seqs"),
+    (dict(Hq=6, Hkv=4), -1, "multiple"),
+    (dict(Hq=34, Hkv=2), -2, "query heads per kv head"),
+    (dict(d=96), -2, "head_dim"),
+    (dict(B=12), -2, "block_size"),
+    (dict(B=128), -2, "block_size"),
+    (dict(MB=0), -1, "max_blocks_per_seq"),
+    (dict(NB=0), -1, "num_blocks"),
+    (dict(scale=float("inf")), -1, "scale"),
+    (dict(pt=24), -1, "partition_tokens"),
+    (dict(pt=16, B=32), -1, "partition_tokens"),
+    (dict(pt=32768), -2, "partition_tokens"),
+    (dict(pt=8192, B=1), -2, "table entries"),
+    (dict(out=None), -1, "NULL"),
+    (dict(query=FAKE + 8), -1, "aligned"),
+    (dict(bt=FAKE + 2), -1, "aligned"),
+    (dict(MB=4096, pt=512), -3, "workspace"),
+    (dict(MB=4096, pt=512, ws=FAKE, wsb=100), -3, "workspace"),
+])
+def test_decode_rejects_bad_arguments(lib, kw, code, msg):
+    assert _decode(lib, **kw) == code
+    assert msg in pa.last_error()
+
+
+def test_decode_zero_sequences_is_a_no_op(lib):
+    assert _decode(lib, S=0, out=None, query=None) == 0
+    assert pa.last_error() == ""
+
+
+def _write(lib, **kw):
+    a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, slots=FAKE, T=3, Hkv=2, d=64, B=16, NB=10, dtype=0)
+    a.update(kw)
+    return lib.pa_reshape_and_cache(a["k"], a["v"], a["kc"], a["vc"], a["slots"], a["T"], a["Hkv"],
+                                    a["d"], a["B"], a["NB"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dtype=3), -1, "dtype"),
+    (dict(T=-2), -1, "num_tokens"),
+    (dict(Hkv=0), -1, "num_kv_heads"),
+    (dict(d=32), -2, "head_dim"),
+    (dict(B=0), -2, "block_size"),
+    (dict(NB=0), -1, "num_blocks"),
+    (dict(kc=None), -1, "NULL"),
+    (dict(k=FAKE + 4), -1, "aligned"),
+    (dict(slots=FAKE + 4), -1, "aligned"),
+])
+def test_cache_write_rejects_bad_arguments(lib, kw, code, msg):
+    assert _write(lib, **kw) == code
+    assert msg in pa.last_error()
+
+
+def test_cache_write_zero_tokens_is_a_no_op(lib):
+    assert _write(lib, T=0, k=None) == 0
+
+
+def test_bad_index_count_rejects_null(lib):
+    assert lib.pa_bad_index_count(None, 0) == -1
+    assert "NULL" in pa.last_error()
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(pa.pagedattn, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.pagedattn.load_library(str(tmp_path / "libpagedattn.so"))

@@ -1,0 +1,87 @@
+"""Full-size workloads on the GPU, in the launch configuration bench.py times.
+
+The oracle computes sampled (sequence, query head) output rows one by one;
+every output row is also checked for properties that hold at any size
+(finite; within the range of the V rows it averages). The step is the one the
+benchmark runs: write each sequence's newest token with pa_reshape_and_cache,
+then pa_decode over the whole sequence.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import paged_kv_cache_305_gb300 as pa
+import workloads as W
+from gpu_util import ATOL, DeviceCase, host_bits, max_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_305_gb300 import build
+    build.build()
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def _pairs(case, n_random=40, seed=0):
+    rng = np.random.default_rng(seed)
+    L = case.seq_lens
+    seqs = {int(np.argmax(L)), int(np.argmin(L)), int(np.argsort(L)[len(L) // 2])}
+    Hq, G = case.num_q_heads, case.group
+    pairs = set()
+    for s in seqs:
+        for hq in {0, G - 1, Hq - 1, int(rng.integers(Hq))}:
+            pairs.add((s, hq))
+    while len(pairs) < len(seqs) * 4 + n_random:
+        pairs.add((int(rng.integers(case.num_seqs)), int(rng.integers(Hq))))
+    return sorted(pairs)
+
+
+def _run_and_check(case):
+    dc = DeviceCase(case)
+    out = dc.step()
+    torch.cuda.synchronize()
+    got = host_bits(out)
+    # the written rows are where the oracle's write puts them
+    B = case.block_size
+    for s in range(case.num_seqs):
+        sl = int(case.slot_mapping[s])
+        if sl >= 0:
+            assert np.array_equal(host_bits(dc.key_cache[sl // B, sl % B]), case.new_key[s])
+            assert np.array_equal(host_bits(dc.value_cache[sl // B, sl % B]), case.new_value[s])
+    kc, vc = oracle.reshape_and_cache(case.new_key, case.new_value, case.key_cache,
+                                      case.value_cache, case.slot_mapping, B, in_place=True)
+    del dc
+    torch.cuda.empty_cache()
+    pairs = _pairs(case)
+    ref = oracle.paged_decode_pairs(case.query, kc, vc, case.block_tables, case.seq_lens, B,
+                                    case.scale, case.dtype, pairs)
+    sel = np.stack([got[s, h] for s, h in pairs])
+    err = max_err(sel, ref, case.dtype)
+    assert err <= ATOL, f"{case.name}: max err {err} over {len(pairs)} sampled rows"
+    full = oracle.to_float64(got, case.dtype)
+    assert np.all(np.isfinite(full))
+    vmax = float(np.max(np.abs(oracle.to_float64(case.value_cache[:: max(1, case.num_blocks // 64)],
+                                                 case.dtype))))
+    assert np.max(np.abs(full)) <= max(vmax, 8.0)
+    if case.dtype == "bf16":
+        # bf16 output rounding stays below the tolerance only for |o| < 0.5
+        assert np.max(np.abs(ref)) < 0.5
+    return err
+
+
+@pytest.mark.parametrize("name", ["llama2_7b_mha", "llama3_8b_gqa", "long_context_splitk"])
+def test_full_size_workload(name):
+    _run_and_check(W.make_workload(name))
+
+
+@pytest.mark.parametrize("B", W.SHARED_PREFIX_BLOCK_SIZES)
+def test_shared_prefix_block_size_sweep(B):
+    _run_and_check(W.make_workload("shared_prefix", block_size=B))
