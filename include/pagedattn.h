@@ -24,7 +24,7 @@
  *
  * Layouts (S = num_seqs, Hq / Hkv = query / kv heads, d = head_dim,
  * B = block_size, NB = num_blocks, MB = max_blocks_per_seq):
- *   query, out          [S, Hq, d]
+ *   query, out          [S, Hq, d]       (out: dtype or fp32, see pa_decode)
  *   key_cache,
  *   value_cache         [NB, B, Hkv, d]   (the physical block pool)
  *   block_tables        [S, MB] int32     (physical block ids)
@@ -44,7 +44,7 @@
 extern "C" {
 #endif
 
-typedef enum { PA_FLOAT16 = 0, PA_BFLOAT16 = 1 } pa_dtype;
+typedef enum { PA_FLOAT16 = 0, PA_BFLOAT16 = 1, PA_FLOAT32 = 2 } pa_dtype;
 
 enum {
   PA_OK = 0,
@@ -99,12 +99,18 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  *   out[s, hq, :] = sum_t softmax(score)_t * V_t
  * where K_t / V_t = key_cache / value_cache[block_tables[s, t / B], t % B, h, :].
  * Slots at or past L and table entries at or past ceil(L / B) are never read.
- * L = 0 gives a zero output row. The output is rounded to `dtype` (nearest
- * even); arithmetic is fp32 with 16-bit (dtype) products.
+ * L = 0 gives a zero output row. Arithmetic is fp32; the q.K and P.V
+ * products take 16-bit (dtype) operands with fp32 accumulation, the softmax
+ * weights being rounded to dtype before the P.V product.
+ *
+ * dtype (PA_FLOAT16 or PA_BFLOAT16) is the type of query and the caches.
+ * out_dtype is either dtype (out is rounded to it, nearest even) or
+ * PA_FLOAT32 (out holds the fp32 result before that rounding; the 16-bit
+ * output of the same call is exactly its nearest-even rounding).
  *
  * The first twelve parameters follow the statement of the problem; the rest
  * give the table's row stride (max_blocks_per_seq), the pool size for index
- * checks (num_blocks), the split-K partition length, the element type, the
+ * checks (num_blocks), the split-K partition length, the element types, the
  * scratch space and the stream.
  *
  * Split-K: each sequence is cut into partitions of partition_tokens tokens
@@ -129,7 +135,7 @@ int pa_decode(void* out, const void* query,
               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
               int block_size, float scale,
               int max_blocks_per_seq, int num_blocks, int partition_tokens,
-              pa_dtype dtype, void* workspace, size_t workspace_bytes,
+              pa_dtype dtype, pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
               cudaStream_t stream);
 
 /*

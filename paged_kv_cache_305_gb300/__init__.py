@@ -6,6 +6,7 @@ The computation lives in ``libpagedattn.so`` (C ABI in ``include/pagedattn.h``);
 from .pagedattn import (  # noqa: F401
     PA_BFLOAT16,
     PA_FLOAT16,
+    PA_FLOAT32,
     PagedAttnError,
     alloc_workspace,
     bad_index_count,

@@ -172,10 +172,13 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
               const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
               int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
               int max_blocks_per_seq, int num_blocks, int partition_tokens, pa_dtype dtype,
-              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+              pa_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   g_error.clear();
   int rc = check_dtype(dtype);
   if (rc != PA_OK) return rc;
+  if (out_dtype != dtype && out_dtype != PA_FLOAT32)
+    return fail(PA_ERR_INVALID, "out_dtype %d must equal dtype %d or be PA_FLOAT32", (int)out_dtype,
+                (int)dtype);
   if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d < 0", num_seqs);
   if (num_q_heads < 1 || num_kv_heads < 1)
     return fail(PA_ERR_INVALID, "num_q_heads %d / num_kv_heads %d must be >= 1", num_q_heads,
@@ -240,6 +243,7 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
   a.partition_tokens = pt;
   a.max_partitions = parts;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
   char* ws = static_cast<char*>(workspace);
   a.ws_count = wl.total ? reinterpret_cast<int*>(ws + wl.count_off) : nullptr;
   a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;

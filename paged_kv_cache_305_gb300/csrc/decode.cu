@@ -301,7 +301,6 @@ paged_decode_kernel(const DecodeArgs a) {
 
   const size_t row0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G;
   if (nparts == 1) {
-    T* og = static_cast<T*>(a.out) + row0 * D;
     for (int i = tid; i < G * (D / 2); i += kThreads) {
       const int g = i / (D / 2), c = 2 * (i % (D / 2));
       float v0 = 0.f, v1 = 0.f;
@@ -313,7 +312,12 @@ paged_decode_kernel(const DecodeArgs a) {
         v1 += f * sO[g * Geo::kOStride + c + 1];
       }
       const float inv = sFac[kWarps * kRows + g];
-      *reinterpret_cast<uint32_t*>(og + g * D + c) = Ty::pack(v0 * inv, v1 * inv);
+      const size_t o_idx = (row0 + g) * D + c;
+      if (a.out_f32) {
+        *reinterpret_cast<float2*>(static_cast<float*>(a.out) + o_idx) = make_float2(v0 * inv, v1 * inv);
+      } else {
+        *reinterpret_cast<uint32_t*>(static_cast<T*>(a.out) + o_idx) = Ty::pack(v0 * inv, v1 * inv);
+      }
     }
     return;
   }
@@ -382,11 +386,17 @@ paged_decode_kernel(const DecodeArgs a) {
     }
     __syncthreads();
   }
-  T* og = static_cast<T*>(a.out) + row0 * D;
 #pragma unroll
   for (int k = 0; k < kAcc; ++k) {
     const int g = gfirst + k * kGStride;
-    if (g < G) og[g * D + col] = Ty::cvt(acc[k]);
+    if (g < G) {
+      const size_t o_idx = (row0 + g) * D + col;
+      if (a.out_f32) {
+        static_cast<float*>(a.out)[o_idx] = acc[k];
+      } else {
+        static_cast<T*>(a.out)[o_idx] = Ty::cvt(acc[k]);
+      }
+    }
   }
   if (tid == 0) *counter = 0;  // ready for the next call on this workspace
 }

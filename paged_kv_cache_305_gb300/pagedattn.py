@@ -17,7 +17,7 @@ import torch
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedattn.so")
 
-PA_FLOAT16, PA_BFLOAT16 = 0, 1
+PA_FLOAT16, PA_BFLOAT16, PA_FLOAT32 = 0, 1, 2
 _DTYPES = {torch.float16: PA_FLOAT16, torch.bfloat16: PA_BFLOAT16}
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_last_error", "pa_bad_index_count")
@@ -47,7 +47,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.pa_decode_workspace_bytes.restype = sz
     L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
-                            i32, i32, i32, i32, vp, sz, vp]
+                            i32, i32, i32, i32, i32, vp, sz, vp]
     L.pa_decode.restype = i32
     L.pa_last_error.argtypes = []
     L.pa_last_error.restype = ctypes.c_char_p
@@ -128,15 +128,16 @@ def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
     """Paged decode attention into ``out`` [S, Hq, d]; returns ``out``.
 
     ``query`` [S, Hq, d]; caches [NB, B, Hkv, d]; ``block_tables`` [S, MB]
-    int32; ``seq_lens`` [S] int32. ``scale`` defaults to 1/sqrt(d). The
-    workspace, when one is needed, comes from :func:`alloc_workspace` (zeroed
-    once, reusable across calls on one stream).
+    int32; ``seq_lens`` [S] int32. ``scale`` defaults to 1/sqrt(d). ``out``
+    has the query's dtype (rounded result) or float32 (the result before that
+    rounding). The workspace, when one is needed, comes from
+    :func:`alloc_workspace` (zeroed once, reusable across calls on one stream).
     """
     S, Hq, d = query.shape
     NB, B, Hkv, d2 = key_cache.shape
     _need(d2 == d and value_cache.shape == key_cache.shape, "cache shape mismatch")
-    _need(out.shape == query.shape and out.dtype == query.dtype == key_cache.dtype == value_cache.dtype,
-          "out/query/cache dtype or shape mismatch")
+    _need(out.shape == query.shape and query.dtype == key_cache.dtype == value_cache.dtype
+          and out.dtype in (query.dtype, torch.float32), "out/query/cache dtype or shape mismatch")
     _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
           "block_tables and seq_lens must be int32")
     _need(block_tables.dim() == 2 and block_tables.shape[0] == S and seq_lens.shape == (S,),
@@ -153,7 +154,9 @@ def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
         _check(L.pa_decode(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
                            value_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(),
                            S, Hq, Hkv, d, B, float(scale), block_tables.shape[1], NB,
-                           partition_tokens, _dtype_code(query), ws_ptr, ws_bytes,
+                           partition_tokens, _dtype_code(query),
+                           PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+                           ws_ptr, ws_bytes,
                            _stream(query, stream)))
     return out
 

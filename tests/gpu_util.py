@@ -35,6 +35,7 @@ class DeviceCase:
         self.new_value = dev_bits(case.new_value, dt, device)
         self.slot_mapping = torch.from_numpy(case.slot_mapping).to(device)
         self.out = torch.empty_like(self.query)
+        self.out32 = torch.empty(self.query.shape, dtype=torch.float32, device=device)
         self.partition_tokens = case.partition_tokens
         self.workspace = pa.alloc_workspace(self.query, self.key_cache, self.block_tables,
                                             case.partition_tokens)
@@ -43,14 +44,16 @@ class DeviceCase:
         pa.reshape_and_cache(self.new_key, self.new_value, self.key_cache, self.value_cache,
                              self.slot_mapping)
 
-    def decode(self, partition_tokens=None, workspace=None):
+    def decode(self, partition_tokens=None, workspace=None, out_f32=False):
+        """Run pa_decode; returns ``out`` (input dtype) or ``out32`` (fp32)."""
         pt = self.partition_tokens if partition_tokens is None else partition_tokens
         ws = self.workspace if partition_tokens is None else workspace
         if partition_tokens is not None and ws is None:
             ws = pa.alloc_workspace(self.query, self.key_cache, self.block_tables, pt)
-        pa.decode(self.out, self.query, self.key_cache, self.value_cache, self.block_tables,
+        out = self.out32 if out_f32 else self.out
+        pa.decode(out, self.query, self.key_cache, self.value_cache, self.block_tables,
                   self.seq_lens, self.case.scale, pt, ws)
-        return self.out
+        return out
 
     def step(self):
         """One decode step: write the new token's K/V, then attend over the sequence."""
@@ -62,6 +65,26 @@ def oracle_after_write(case):
     """Oracle caches after the step's cache write (host copies)."""
     return oracle.reshape_and_cache(case.new_key, case.new_value, case.key_cache,
                                     case.value_cache, case.slot_mapping, case.block_size)
+
+
+def check_parity(out16: np.ndarray, out32: np.ndarray, ref: np.ndarray, dtype: str,
+                 what: str = "") -> float:
+    """The two-part parity bar for decode.
+
+    1. The fp32 result is within ATOL of the float64 oracle.
+    2. The 16-bit output is exactly the nearest-even rounding of that fp32
+       result (so its distance from the oracle is the fp32 error plus at most
+       half a unit in the last place of the 16-bit type).
+    Returns the fp32 error.
+    """
+    o32 = np.asarray(out32, dtype=np.float64)
+    assert np.all(np.isfinite(o32)), f"{what}: non-finite output"
+    err = float(np.max(np.abs(o32 - ref))) if ref.size else 0.0
+    assert err <= ATOL, f"{what}: max |fp32 - oracle| = {err}"
+    rounded = oracle.round_to_dtype(o32, dtype)
+    bad = int(np.sum(rounded != out16))
+    assert bad == 0, f"{what}: {bad} 16-bit outputs differ from the rounding of the fp32 result"
+    return err
 
 
 def max_err(got_bits: np.ndarray, ref: np.ndarray, dtype: str) -> float:

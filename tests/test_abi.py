@@ -65,15 +65,17 @@ FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced by thes
 
 def _decode(lib, **kw):
     a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, S=2, Hq=8, Hkv=2, d=128,
-             B=16, scale=0.1, MB=4, NB=100, pt=0, dtype=1, ws=None, wsb=0)
+             B=16, scale=0.1, MB=4, NB=100, pt=0, dtype=1, odt=None, ws=None, wsb=0)
     a.update(kw)
     return lib.pa_decode(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["sl"], a["S"], a["Hq"],
                          a["Hkv"], a["d"], a["B"], a["scale"], a["MB"], a["NB"], a["pt"], a["dtype"],
-                         a["ws"], a["wsb"], None)
+                         a["dtype"] if a["odt"] is None else a["odt"], a["ws"], a["wsb"], None)
 
 
 @pytest.mark.parametrize("kw,code,msg", [
     (dict(dtype=5), -1, "dtype"),
+    (dict(dtype=2), -1, "dtype"),
+    (dict(odt=0), -1, "out_dtype"),
     (dict(S=-1), -1, "num_seqs"),
     (dict(Hq=6, Hkv=4), -1, "multiple"),
     (dict(Hq=34, Hkv=2), -2, "query heads per kv head"),

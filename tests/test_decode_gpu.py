@@ -18,7 +18,8 @@ torch = pytest.importorskip("torch")
 import oracle
 import paged_kv_cache_305_gb300 as pa
 import workloads as W
-from gpu_util import ATOL, DeviceCase, dev_bits, host_bits, max_err, oracle_after_write
+from gpu_util import (ATOL, DeviceCase, check_parity, dev_bits, host_bits, max_err,
+                      oracle_after_write)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,15 +35,21 @@ def _cuda():
     torch.cuda.synchronize()
 
 
-def _check_step(case, pt=None):
+def _parity(dc, ref, pt=None, what=""):
+    """Run the 16-bit and the fp32 output of the same decode and apply the parity bar."""
+    out16 = host_bits(dc.decode(pt)).copy()
+    out32 = dc.decode(pt, out_f32=True).cpu().numpy()
+    check_parity(out16, out32, ref, dc.case.dtype, what or dc.case.name)
+    return out16
+
+
+def _check_step(case):
     dc = DeviceCase(case)
-    out = dc.step() if pt is None else (dc.write_new_tokens(), dc.decode(pt))[1]
-    torch.cuda.synchronize()
+    dc.write_new_tokens()
     kc, vc = oracle_after_write(case)
     ref = oracle.paged_decode(case.query, kc, vc, case.block_tables, case.seq_lens,
                               case.block_size, case.scale, case.dtype)
-    err = max_err(host_bits(out), ref, case.dtype)
-    assert err <= ATOL, f"{case.name}: max err {err}"
+    _parity(dc, ref)
     return dc, ref
 
 
@@ -104,6 +111,14 @@ def test_worked_example_in_head_dim_64():
     got = oracle.to_float64(host_bits(out), dt)[0, 0]
     assert abs(got[0] - 4.125619931152994) <= ATOL and abs(got[1] - 4.125619931152994) <= ATOL
     assert np.all(got[2:] == 0)
+    out32 = torch.empty((1, 1, d), dtype=torch.float32, device="cuda")
+    pa.decode(out32, dev_bits(W.f32_to_bits(q, dt), dt), dev_bits(W.f32_to_bits(kc, dt), dt),
+              dev_bits(W.f32_to_bits(vc, dt), dt),
+              torch.tensor([g["block_table"]], dtype=torch.int32, device="cuda"),
+              torch.tensor([g["seq_len"]], dtype=torch.int32, device="cuda"), scale=1.0)
+    ref = np.zeros((1, 1, d))
+    ref[0, 0, :2] = 4.125619931152994
+    check_parity(host_bits(out), out32.cpu().numpy(), ref, dt, "worked example")
     # the page's printed code output, 4.1256 to 4 decimals
     assert abs(got[0] - g["printed"]["output_code_4dp"][0]) <= ATOL
 
@@ -129,7 +144,7 @@ def test_zero_length_writes_zeros():
     assert np.all(got[0] == 0) and np.all(got[2] == 0)
     ref = oracle.paged_decode(case.query, case.key_cache, case.value_cache, case.block_tables,
                               case.seq_lens, 16, case.scale, "bf16")
-    assert max_err(got, ref, "bf16") <= ATOL
+    _parity(dc, ref, 64)
 
 
 def test_unused_slots_and_table_tail_are_never_read():
@@ -160,10 +175,9 @@ def test_placement_independence_bit_exact():
 def test_shared_blocks_bit_exact_vs_private():
     case = W.shared_prefix_case(block_size=16, groups=3, per_group=4, prefix=256,
                                 suffix_range=(0, 300), num_heads=4, head_dim=128, seed=2)
-    shared = host_bits(DeviceCase(case).decode())
     ref = oracle.paged_decode(case.query, case.key_cache, case.value_cache, case.block_tables,
                               case.seq_lens, 16, case.scale, "fp16")
-    assert max_err(shared, ref, "fp16") <= ATOL
+    shared = _parity(DeviceCase(case), ref)
     B = 16
     ks, vs, tables = [], [], np.zeros_like(case.block_tables)
     for s in range(case.num_seqs):
@@ -189,7 +203,7 @@ def test_repeatable_and_workspace_reusable():
     assert int(ws[: case.num_seqs * case.num_q_heads * 4].view(torch.int32).abs().sum()) == 0
     ref = oracle.paged_decode(case.query, case.key_cache, case.value_cache, case.block_tables,
                               case.seq_lens, 16, case.scale, "bf16")
-    assert max_err(a, ref, "bf16") <= ATOL
+    assert np.array_equal(_parity(dc, ref), a)
 
 
 def test_partition_length_does_not_change_the_result():
@@ -200,9 +214,8 @@ def test_partition_length_does_not_change_the_result():
     dc = DeviceCase(case)
     outs = []
     for pt in (16, 64, 512, 4096, 16384):
-        got = host_bits(dc.decode(partition_tokens=pt)).copy()
-        assert max_err(got, ref, "bf16") <= ATOL, pt
-        outs.append(oracle.to_float64(got, "bf16"))
+        _parity(dc, ref, pt, f"partition_tokens={pt}")
+        outs.append(dc.out32.cpu().numpy().astype(np.float64))
     for o in outs[1:]:
         assert np.max(np.abs(o - outs[0])) <= ATOL
 
@@ -218,7 +231,11 @@ def test_runs_on_a_side_stream():
     kc, vc = oracle_after_write(case)
     ref = oracle.paged_decode(case.query, kc, vc, case.block_tables, case.seq_lens, 16,
                               case.scale, "fp16")
-    assert max_err(host_bits(dc.out), ref, "fp16") <= ATOL
+    out16 = host_bits(dc.out).copy()
+    with torch.cuda.stream(st):
+        dc.decode(out_f32=True)
+    st.synchronize()
+    check_parity(out16, dc.out32.cpu().numpy(), ref, "fp16", "side stream")
 
 
 def test_bad_indices_are_counted_not_faulted():
