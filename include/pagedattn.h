@@ -99,9 +99,10 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  *   out[s, hq, :] = sum_t softmax(score)_t * V_t
  * where K_t / V_t = key_cache / value_cache[block_tables[s, t / B], t % B, h, :].
  * Slots at or past L and table entries at or past ceil(L / B) are never read.
- * L = 0 gives a zero output row. Arithmetic is fp32; the q.K and P.V
- * products take 16-bit (dtype) operands with fp32 accumulation, the softmax
- * weights being rounded to dtype before the P.V product.
+ * L = 0 gives a zero output row. Arithmetic is fp32: q.K takes the 16-bit
+ * inputs with fp32 accumulation; each softmax weight enters P.V as the sum of
+ * two 16-bit (dtype) parts (its rounding and the rounding of the remainder),
+ * again with fp32 accumulation.
  *
  * dtype (PA_FLOAT16 or PA_BFLOAT16) is the type of query and the caches.
  * out_dtype is either dtype (out is rounded to it, nearest even) or

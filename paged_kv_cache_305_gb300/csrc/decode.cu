@@ -18,7 +18,8 @@
 // barrier. Per tile a warp computes the scores of 16 query-head rows (the
 // group, zero-padded) against 16 tokens with m16n8k16 tensor-core products,
 // updates the online softmax in fp32 (base-2 exponent), and accumulates
-// P.V with the same instruction. The 4 warps' states are then merged by
+// P.V with the same instruction (weights as a 16-bit head plus a 16-bit
+// remainder, so their rounding stays far below the output tolerance). The 4 warps' states are then merged by
 // log-sum-exp; a partition that is not a sequence's only one stores
 // (normalised output, lse) to the workspace, and the last partition CTA of a
 // (sequence, kv head) to arrive merges all partitions and writes `out`.
@@ -223,18 +224,31 @@ paged_decode_kernel(const DecodeArgs a) {
     const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
     m0 = n0;
     m1 = n1;
-    uint32_t pa[4];
-    pa[0] = Ty::pack(ex2(x[0] - n0), ex2(x[1] - n0));
-    pa[1] = Ty::pack(ex2(x[4] - n1), ex2(x[5] - n1));
-    pa[2] = Ty::pack(ex2(x[2] - n0), ex2(x[3] - n0));
-    pa[3] = Ty::pack(ex2(x[6] - n1), ex2(x[7] - n1));
-    // the sums use the rounded weights that enter the P.V product
-    {
-      const float2 p0 = Ty::unpack(pa[0]), p2 = Ty::unpack(pa[2]);
-      const float2 p1 = Ty::unpack(pa[1]), p3 = Ty::unpack(pa[3]);
-      l0 = l0 * al0 + ((p0.x + p0.y) + (p2.x + p2.y));
-      l1 = l1 * al1 + ((p1.x + p1.y) + (p3.x + p3.y));
+    // weights, as A fragments: rows lane/4 (pa[0], pa[2]) and lane/4 + 8 (pa[1], pa[3]).
+    // Each fp32 weight is split into a 16-bit head and the 16-bit rounding of
+    // the remainder; both go through the P.V product, so the weights carry
+    // about 16 significant bits instead of the input type's 8 or 11.
+    float p[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      p[j] = ex2(x[j] - n0);
+      p[j + 4] = ex2(x[j + 4] - n1);
     }
+    uint32_t pa[4], pl[4];
+    pa[0] = Ty::pack(p[0], p[1]);
+    pa[1] = Ty::pack(p[4], p[5]);
+    pa[2] = Ty::pack(p[2], p[3]);
+    pa[3] = Ty::pack(p[6], p[7]);
+    {
+      const int src[4][2] = {{0, 1}, {4, 5}, {2, 3}, {6, 7}};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 hd = Ty::unpack(pa[j]);
+        pl[j] = Ty::pack(p[src[j][0]] - hd.x, p[src[j][1]] - hd.y);
+      }
+    }
+    l0 = l0 * al0 + ((p[0] + p[1]) + (p[2] + p[3]));
+    l1 = l1 * al1 + ((p[4] + p[5]) + (p[6] + p[7]));
     if (__any_sync(0xffffffffu, (al0 != 1.f) | (al1 != 1.f))) {
 #pragma unroll
       for (int n = 0; n < kNTiles; ++n) {
@@ -254,6 +268,8 @@ paged_decode_kernel(const DecodeArgs a) {
         ldmatrix_x4_trans(b, smem_u32(sv + tok * kRowBytes + swz(tok, 2 * j + (mi >> 1))));
         Ty::mma(o[2 * j], pa, b[0], b[1]);
         Ty::mma(o[2 * j + 1], pa, b[2], b[3]);
+        Ty::mma(o[2 * j], pl, b[0], b[1]);
+        Ty::mma(o[2 * j + 1], pl, b[2], b[3]);
       }
     }
   }
