@@ -183,7 +183,7 @@ def cpu_baseline_block(case, budget_s):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    case = W.make_workload(args.workload, seed=0, block_size=args.block_size)
+    case = W.make_workload(args.workload, seed=0, block_size=args.block_size, num_seqs=args.num_seqs)
     oracle_prepare(case)
     # every step is a bounded sample, sized so that warm-up + steps take ~2 minutes
     per_step = max(0.002, min(args.ref_budget, 120.0 / max(1, args.steps + args.warmup)))
@@ -242,7 +242,7 @@ def run_ours(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
 
-    case = W.make_workload(args.workload, seed=rank,
+    case = W.make_workload(args.workload, seed=rank, num_seqs=args.num_seqs,
                            block_size=args.block_size if args.workload == "shared_prefix" else None)
     pt = args.partition_tokens if args.partition_tokens is not None else case.partition_tokens
     tdt = {"fp16": torch.float16, "bf16": torch.bfloat16}[case.dtype]
@@ -357,8 +357,9 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_block(W.make_workload(args.workload, seed=0,
-                                                  block_size=args.block_size), args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline_block(
+            W.make_workload(args.workload, seed=0, block_size=args.block_size,
+                            num_seqs=args.num_seqs), args.cpu_budget)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -373,6 +374,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(W.WORKLOADS) + ["shared_prefix"])
     ap.add_argument("--block-size", type=int, default=16, help="shared_prefix only")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="shrink the batch (small profiling captures only)")
     ap.add_argument("--partition-tokens", type=int, default=None)
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget", type=float, default=20.0)

@@ -295,11 +295,18 @@ SHARED_PREFIX_BLOCK_SIZES = (1, 8, 16, 32, 64)
 
 
 def make_workload(name: str, seed: int = 0, block_size: Optional[int] = None,
-                  threads=None) -> DecodeCase:
-    """Build one of the named workloads (``shared_prefix`` needs ``block_size``)."""
+                  threads=None, num_seqs: Optional[int] = None) -> DecodeCase:
+    """Build one of the named workloads (``shared_prefix`` takes ``block_size``).
+
+    ``num_seqs`` shrinks the batch (same per-sequence recipe), for profiling
+    captures that must stay small.
+    """
     if name == "shared_prefix":
-        return shared_prefix_case(block_size=block_size or 16, seed=seed, threads=threads)
+        kw = {} if num_seqs is None else {"groups": max(1, num_seqs // 8)}
+        return shared_prefix_case(block_size=block_size or 16, seed=seed, threads=threads, **kw)
     kw = dict(WORKLOADS[name])
+    if num_seqs is not None:
+        kw["num_seqs"] = num_seqs
     return random_case(seed=seed, name=name, threads=threads, **kw)
 
 
