@@ -140,6 +140,42 @@ int pa_decode(void* out, const void* query,
               cudaStream_t stream);
 
 /*
+ * pa_decode without a caller-provided workspace, for callers that cannot
+ * allocate device memory: for example a plugin inside a host runtime that owns
+ * every device allocation, or a serving loop that forbids allocation after
+ * start-up (cudaMalloc can synchronise the device and can fail under memory
+ * pressure). The pages describe no such entry point; it has no counterpart
+ * there.
+ *
+ * Arguments, results and errors are those of pa_decode, without `workspace`
+ * and `workspace_bytes`. The split-K scratch is a fixed array of
+ * pa_decode_no_alloc_scratch_bytes() bytes (64 MiB) that the library keeps in
+ * device memory; every GPU that loads the library holds it until the process
+ * exits. Sizes whose pa_decode_workspace_bytes(...) exceed it are rejected
+ * with PA_ERR_WORKSPACE.
+ *
+ * Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * Its first call on a device (with that device current) looks up the array's
+ * device address with cudaGetSymbolAddress and caches it; make that first call
+ * before any stream capture. Each call clears the scratch's arrival counters
+ * with cudaMemsetAsync on `stream`, then runs pa_decode on it.
+ *
+ * All calls on a device share the one array, which keeps the previous call's
+ * contents: calls that can overlap on the GPU (other streams, other threads)
+ * race on it and give wrong results. Serialise them.
+ */
+int pa_decode_no_alloc(void* out, const void* query,
+                       const void* key_cache, const void* value_cache,
+                       const int32_t* block_tables, const int32_t* seq_lens,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, float scale,
+                       int max_blocks_per_seq, int num_blocks, int partition_tokens,
+                       pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch that pa_decode_no_alloc uses. */
+size_t pa_decode_no_alloc_scratch_bytes(void);
+
+/*
  * Message for the most recent non-OK return on the calling thread ("" if
  * none). The pointer stays valid until the next library call on that thread.
  */

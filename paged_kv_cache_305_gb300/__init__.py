@@ -11,8 +11,10 @@ from .pagedattn import (  # noqa: F401
     alloc_workspace,
     bad_index_count,
     decode,
+    decode_no_alloc,
     decode_workspace_bytes,
     last_error,
     load_library,
+    no_alloc_scratch_bytes,
     reshape_and_cache,
 )

@@ -86,6 +86,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 
 namespace pa {
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions) {
   WorkspaceLayout w{};
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;

@@ -36,6 +36,9 @@ struct DecodeArgs {
   unsigned long long* bad;  // device counter of rejected indices
 };
 
+// Records `msg` as the calling thread's last error and returns `code`.
+int set_error(int code, const char* msg);
+
 // Workspace carve-up shared by pa_decode_workspace_bytes and pa_decode.
 struct WorkspaceLayout {
   size_t count_off, lse_off, out_off, total;

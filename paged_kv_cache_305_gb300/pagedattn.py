@@ -20,7 +20,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpagedatt
 PA_FLOAT16, PA_BFLOAT16, PA_FLOAT32 = 0, 1, 2
 _DTYPES = {torch.float16: PA_FLOAT16, torch.bfloat16: PA_BFLOAT16}
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
-            "pa_last_error", "pa_bad_index_count")
+            "pa_last_error", "pa_bad_index_count", "pa_decode_no_alloc",
+            "pa_decode_no_alloc_scratch_bytes")
 
 _lib = None
 
@@ -53,6 +54,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_last_error.restype = ctypes.c_char_p
     L.pa_bad_index_count.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
     L.pa_bad_index_count.restype = i32
+    L.pa_decode_no_alloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                     ctypes.c_float, i32, i32, i32, i32, i32, vp]
+    L.pa_decode_no_alloc.restype = i32
+    L.pa_decode_no_alloc_scratch_bytes.argtypes = []
+    L.pa_decode_no_alloc_scratch_bytes.restype = sz
     _lib = L
     return L
 
@@ -166,3 +172,44 @@ def bad_index_count(clear: bool = False) -> int:
     n = ctypes.c_ulonglong(0)
     _check(load_library().pa_bad_index_count(ctypes.byref(n), int(bool(clear))))
     return int(n.value)
+
+
+def decode_no_alloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                    value_cache: torch.Tensor, block_tables: torch.Tensor,
+                    seq_lens: torch.Tensor, scale: Optional[float] = None,
+                    partition_tokens: int = 0, stream=None) -> torch.Tensor:
+    """:func:`decode` for callers that cannot allocate device memory.
+
+    The split-K scratch is the library's own fixed device array
+    (:func:`no_alloc_scratch_bytes` bytes), so no workspace is passed and
+    nothing is allocated. Calls that may overlap on the GPU share that array
+    and must be serialised by the caller.
+    """
+    S, Hq, d = query.shape
+    NB, B, Hkv, d2 = key_cache.shape
+    _need(d2 == d and value_cache.shape == key_cache.shape, "cache shape mismatch")
+    _need(out.shape == query.shape and query.dtype == key_cache.dtype == value_cache.dtype
+          and out.dtype in (query.dtype, torch.float32), "out/query/cache dtype or shape mismatch")
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S and seq_lens.shape == (S,),
+          "block_tables/seq_lens shape mismatch")
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    L = load_library()
+    with torch.cuda.device(query.device):
+        _check(L.pa_decode_no_alloc(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
+                                    value_cache.data_ptr(), block_tables.data_ptr(),
+                                    seq_lens.data_ptr(), S, Hq, Hkv, d, B, float(scale),
+                                    block_tables.shape[1], NB, partition_tokens,
+                                    _dtype_code(query),
+                                    PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+                                    _stream(query, stream)))
+    return out
+
+
+def no_alloc_scratch_bytes() -> int:
+    """Bytes of the fixed split-K scratch behind :func:`decode_no_alloc`."""
+    return int(load_library().pa_decode_no_alloc_scratch_bytes())
