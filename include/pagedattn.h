@@ -116,10 +116,13 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  *
  * Split-K: each sequence is cut into partitions of partition_tokens tokens
  * (0 = default 512; otherwise a multiple of 16 and of block_size, at most
- * 16384, and at most 4096 table entries long). Each partition's result is
- * combined by log-sum-exp inside the same kernel launch, so the call is a
- * single kernel. `workspace` must hold pa_decode_workspace_bytes(...) bytes
- * (it may be NULL when that is 0); see there for the zeroing rule.
+ * 2^20). The kernel is persistent (a few CTAs per SM); each CTA takes a
+ * contiguous, token-balanced run of partitions and continues the online
+ * softmax across consecutive partitions of one (sequence, kv head). Where a
+ * sequence's partitions are split between CTAs, the pieces are combined by
+ * log-sum-exp inside the same launch, so the call is a single kernel.
+ * `workspace` must hold pa_decode_workspace_bytes(...) bytes (it may be NULL
+ * when that is 0); see there for the zeroing rule.
  *
  * Sizes: num_seqs >= 0 (0 is a no-op) and <= 65535, num_kv_heads in
  * [1, 65535], num_q_heads a multiple of num_kv_heads with at most 16 query

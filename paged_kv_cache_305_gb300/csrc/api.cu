@@ -44,6 +44,22 @@ __device__ unsigned long long g_bad_index_count;
 
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long*> g_bad_ptr[kMaxDevices];
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int num_sms(int* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index %d", dev);
+  int n = g_num_sms[dev].load(std::memory_order_acquire);
+  if (n <= 0) {
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(multiprocessor count)");
+    g_num_sms[dev].store(n, std::memory_order_release);
+  }
+  *out = n;
+  return PA_OK;
+}
 
 int bad_counter(unsigned long long** out) {
   int dev = 0;
@@ -74,9 +90,6 @@ int resolve_partition(int partition_tokens, int block_size, int* pt) {
                 p, block_size);
   if (p > pa::kMaxPartitionTokens)
     return fail(PA_ERR_UNSUPPORTED, "partition_tokens %d > %d", p, pa::kMaxPartitionTokens);
-  if (p / block_size > pa::kMaxTableEntriesPerPartition)
-    return fail(PA_ERR_UNSUPPORTED, "a partition spans %d table entries (> %d)", p / block_size,
-                pa::kMaxTableEntriesPerPartition);
   *pt = p;
   return PA_OK;
 }
@@ -224,6 +237,17 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
                   workspace == nullptr ? (size_t)0 : workspace_bytes);
     if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
   }
+  int sms = 0;
+  rc = num_sms(&sms);
+  if (rc != PA_OK) return rc;
+  // the persistent schedule works in 64-bit positions: the total weight times
+  // the grid size (at most 32 CTAs per SM) must stay below 2^62
+  {
+    const double wmax = static_cast<double>(num_seqs) * num_kv_heads *
+                        (static_cast<double>(lmax) + static_cast<double>(parts) * pa::kUnitCost);
+    if (wmax * 32.0 * sms >= 4.0e18)
+      return fail(PA_ERR_UNSUPPORTED, "num_seqs * num_kv_heads * max sequence length too large");
+  }
   unsigned long long* bad = nullptr;
   rc = bad_counter(&bad);
   if (rc != PA_OK) return rc;
@@ -251,7 +275,7 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
   a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
   a.ws_out = wl.total ? reinterpret_cast<float*>(ws + wl.out_off) : nullptr;
   a.bad = bad;
-  cudaError_t e = pa::launch_decode(a, head_dim, dtype == PA_BFLOAT16, stream);
+  cudaError_t e = pa::launch_decode(a, head_dim, dtype == PA_BFLOAT16, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
   return PA_OK;
 }

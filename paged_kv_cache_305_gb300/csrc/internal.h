@@ -8,8 +8,7 @@
 namespace pa {
 
 constexpr int kDefaultPartitionTokens = 512;
-constexpr int kMaxPartitionTokens = 16384;
-constexpr int kMaxTableEntriesPerPartition = 4096;
+constexpr int kMaxPartitionTokens = 1 << 20;
 constexpr int kMaxGroup = 16;  // query heads per kv head (rows of one mma tile)
 
 struct DecodeArgs {
@@ -45,9 +44,16 @@ struct WorkspaceLayout {
 };
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions);
 
+// Scheduling of the persistent decode kernel: a partition weighs its tokens
+// plus kUnitCost; a CTA keeps at most kMaxSegments segment records at a time.
+constexpr int kUnitCost = 32;
+constexpr int kMaxSegments = 64;
+
 // Launchers: return a cudaError_t from the launch (cudaSuccess on success).
-cudaError_t launch_decode(const DecodeArgs& a, int head_dim, bool bf16, cudaStream_t stream);
-size_t decode_smem_bytes(int head_dim, int table_entries);
+// `num_sms` is the device's multiprocessor count (the persistent grid is a
+// multiple of it).
+cudaError_t launch_decode(const DecodeArgs& a, int head_dim, bool bf16, int num_sms,
+                          cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int64_t* slot_mapping,

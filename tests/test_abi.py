@@ -87,8 +87,7 @@ def _decode(lib, **kw):
     (dict(scale=float("inf")), -1, "scale"),
     (dict(pt=24), -1, "partition_tokens"),
     (dict(pt=16, B=32), -1, "partition_tokens"),
-    (dict(pt=32768), -2, "partition_tokens"),
-    (dict(pt=8192, B=1), -2, "table entries"),
+    (dict(pt=1 << 21), -2, "partition_tokens"),
     (dict(out=None), -1, "NULL"),
     (dict(query=FAKE + 8), -1, "aligned"),
     (dict(bt=FAKE + 2), -1, "aligned"),
