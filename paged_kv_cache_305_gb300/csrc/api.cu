@@ -263,6 +263,10 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
   a.num_q_heads = num_q_heads;
   a.num_kv_heads = num_kv_heads;
   a.group = group;
+  // One kv head per scheduling unit: grouping 2 or 4 heads per CTA (warps on
+  // adjacent heads) made the units coarser and was never faster at 512-token
+  // partitions on GB300; the kernel keeps the grouping as a parameter.
+  a.heads_per_cta = 1;
   a.block_shift = shift;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_blocks = num_blocks;

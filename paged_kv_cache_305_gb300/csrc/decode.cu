@@ -9,31 +9,37 @@
 // (Optimized CUDA Kernels: attention computed directly on the paged
 // structure, one block at a time, with a running max and running sum).
 //
-// Work decomposition. A "row" is one (sequence, kv head); all G = Hq / Hkv
-// query heads of the kv head are computed together, so every K/V byte is read
-// from HBM once per call. A row is cut into partitions of `partition_tokens`
-// tokens (split-K). The kernel is persistent: a grid of (SMs x CTAs per SM)
-// CTAs, each taking a contiguous run of partitions in (sequence, kv head,
-// partition) order, balanced by tokens (plus a fixed cost per partition).
-// Consecutive partitions of one row inside a CTA form a "segment": the online
-// softmax simply continues across their boundary. A segment that is a whole
-// row writes `out`; a row cut between CTAs leaves one piece per CTA (fp32
-// normalised output + base-2 log-sum-exp) in the workspace, and the last CTA
-// to finish a piece of that row merges the pieces in order and writes `out`.
+// Work decomposition. The G = Hq / Hkv query heads of a kv head are computed
+// together, so every K/V byte is read from HBM once per call. Kv heads are
+// taken in groups of Hc (4, 2 or 1, dividing Hkv); a "row" is one (sequence,
+// head group), cut into partitions of `partition_tokens` tokens (split-K).
+// The kernel is persistent: a grid of (SMs x CTAs per SM) CTAs, each taking a
+// contiguous run of partitions in (sequence, head group, partition) order,
+// balanced by tokens (plus a fixed cost per partition). Consecutive
+// partitions of one row inside a CTA form a "segment": the online softmax
+// simply continues across their boundary. A segment that is a whole row
+// writes `out`; a row cut between CTAs leaves one piece per CTA and head
+// (fp32 normalised output + base-2 log-sum-exp) in the workspace, and the
+// last piece of a head to arrive merges its pieces in order and writes `out`.
 //
-// Inside a CTA, each of the 4 warps owns every 4th 16-token tile of each
-// segment and streams K/V through its own cp.async ring, which runs on across
-// segment boundaries. Table ids are loaded several tiles ahead into registers
-// (one per lane for one of the tile's 16 rows) and handed out by shuffles.
-// Per tile a warp computes the scores of 16 query-head rows (the group,
-// zero-padded) against 16 tokens with m16n8k16 tensor-core products, updates
-// the online softmax in fp32 with base-2 exponents, and accumulates P.V with
-// the same instruction (weights as a 16-bit head plus a 16-bit remainder, so
-// their rounding stays far below the output tolerance). At a segment end the
-// four warps' states are merged by log-sum-exp through shared memory.
+// Inside a CTA the 4 warps are spread over the Hc heads of the group (4 / Hc
+// warps per head, splitting the head's 16-token tiles round-robin), so at any
+// time the warps read the same token slots of adjacent heads: with Hc = 4 one
+// slot's reads are 4 x d x 2 contiguous bytes. Each warp streams K/V through
+// its own cp.async ring, which runs on across segment boundaries; table ids
+// are loaded several tiles ahead into registers (one per lane for one of the
+// tile's 16 rows) and handed out by shuffles. Per 16-token tile a warp
+// computes S^T = K q^T with m16n8k16 tensor-core products (16 tokens x 8 query
+// heads per product, so a group of up to 8 heads costs one product per 16
+// dims), updates the online softmax per head in fp32 with base-2 exponents,
+// transposes the weights in registers (movmatrix) into the B operand, and
+// accumulates O^T = V^T P^T with the same instruction (weights as a 16-bit
+// head plus a 16-bit remainder, so their rounding stays far below the output
+// tolerance). At a segment end a warp that owns its head alone finalizes from
+// registers; warps sharing a head first merge through shared memory.
 //
-// Shared-memory K/V/q rows are 16-byte-chunk XOR swizzled (chunk ^ (row & 7))
-// so the 8 row addresses of every ldmatrix phase fall in distinct banks.
+// Shared-memory K/V rows are 16-byte-chunk XOR swizzled (chunk ^ (row & 7)) so
+// the 8 row addresses of every ldmatrix phase fall in distinct banks.
 #include <cuda_runtime.h>
 #include <limits.h>
 #include <math.h>
@@ -48,11 +54,11 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;  // tokens per warp tile (the k extent of the P.V product)
 constexpr int kRows = 16;        // query-head rows of one tensor-core tile
-constexpr int kIdDepth = 4;      // tiles whose table ids are in flight ahead of their copies
+constexpr int kIdDepth = 8;      // tiles whose table ids are in flight ahead of their copies
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Seg {
-  int s, h;      // sequence, kv head
+  int s, hg;     // sequence, kv-head group
   int t0, t1;    // token range [t0, t1)
   int ntiles;    // 16-token tiles in the range
   int piece;     // -1: the segment is the whole row; else its piece index
@@ -67,14 +73,10 @@ struct Geometry {
   static constexpr int kTileBytes = kTileTokens * kRowBytes;  // 16 rows
   static constexpr int kStageBytes = 2 * kTileBytes;          // K tile + V tile
   static constexpr int kPipeBytes = kWarps * STAGES * kStageBytes;
-  static constexpr int kQBytes = kRows * kRowBytes;
   static constexpr int kMLBytes = kWarps * 2 * kRows * 4;  // per-warp row max and sum
-  static constexpr int kFacBytes = (kWarps + 2) * kRows * 4;
   static constexpr int kSegBytes = kMaxSegments * static_cast<int>(sizeof(Seg));
-  static constexpr int kFixedBytes = kQBytes + kPipeBytes + kMLBytes + kFacBytes + kSegBytes;
+  static constexpr int kFixedBytes = kPipeBytes + kMLBytes + kSegBytes;
   static constexpr int kOStride = D + 4;  // fp32 row stride of a warp's state in the merge area
-  static constexpr int kQRegs = kRows * kChunks / kThreads;  // 16-byte q chunks per thread
-  static_assert(kRows * kChunks % kThreads == 0, "q chunks must divide among threads");
   static_assert(kPipeBytes >= kWarps * 8, "the schedule scan reuses the ring area");
 };
 
@@ -94,15 +96,15 @@ __device__ __forceinline__ long long first_pos(int c, int C, long long W) {
   return static_cast<long long>(c) * q + (static_cast<long long>(c) * r + C - 1) / C;
 }
 
-template <typename Ty, int D, int STAGES>
-__global__ void __launch_bounds__(kThreads)
+template <typename Ty, int D, int STAGES, int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
 paged_decode_kernel(const DecodeArgs a) {
   using Geo = Geometry<D, STAGES>;
   using T = typename Ty::T;
   constexpr int kRowBytes = Geo::kRowBytes;
   constexpr int kChunks = Geo::kChunks;
   constexpr int kKSteps = D / 16;  // k-steps of the q.K product over head_dim
-  constexpr int kNTiles = D / 8;   // n-tiles of the P.V product over head_dim
+  constexpr int kMT = D / 16;      // 16-dim m-tiles of the P.V product over head_dim
   constexpr int kRowsPerCopy = 32 / kChunks;          // rows one warp-wide copy covers
   constexpr int kCopies = kTileTokens / kRowsPerCopy;  // copies per lane per tensor per tile
   constexpr int kOS = Geo::kOStride;
@@ -117,28 +119,30 @@ paged_decode_kernel(const DecodeArgs a) {
   const int G = a.group;
   const int S = a.num_seqs;
   const int Hkv = a.num_kv_heads;
+  const int Hc = a.heads_per_cta;
+  const int NG = Hkv / Hc;          // head groups per sequence (rows per sequence)
+  const int Wh = kWarps / Hc;       // warps per head
+  const int hi = warp / Wh;         // this warp's head within the group
+  const int ws = warp % Wh;         // this warp's share of the head's tiles
   const int Pt = a.partition_tokens;
   const int Lmax = a.max_blocks_per_seq << shift;
   const long long UW = static_cast<long long>(Pt) + kUnitCost;  // weight of a full partition
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* sQ = smem;
-  unsigned char* sPipe = smem + Geo::kQBytes;
+  unsigned char* sPipe = smem;
   float* sML = reinterpret_cast<float*>(sPipe + Geo::kPipeBytes);  // [warp][m|l][row]
-  float* sFac = sML + kWarps * 2 * kRows;  // [warp][row] weights, [row] 1/sum, [row] lse
-  Seg* sSeg = reinterpret_cast<Seg*>(sFac + (kWarps + 2) * kRows);
-  float* sMerge =
+  Seg* sSeg = reinterpret_cast<Seg*>(sML + kWarps * 2 * kRows);
+  float* sMerge =  // [warp][G][kOS], present only when warps share a head
       reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sSeg) + Geo::kSegBytes);
   __shared__ long long sW[3];  // base position of the first / last unit's sequence
-  __shared__ int sRange[6];    // first unit (s, h, p), end unit (s, h, p)
-  __shared__ int sFlag;
+  __shared__ int sRange[6];    // first unit (s, hg, p), end unit (s, hg, p)
 
   auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > Lmax ? Lmax : L); };
   auto nparts_of = [&](int L) { return L > 0 ? (L + Pt - 1) / Pt : 1; };
 
   // ======================= schedule ========================================
   // Every CTA computes the same prefix of sequence weights: a sequence of
-  // length L has ceil(L / Pt) partitions per kv head (one if L is 0), each
+  // length L has ceil(L / Pt) partitions per head group (one if L is 0), each
   // weighing its tokens plus kUnitCost. CTA c owns the partitions whose start
   // position lies in [first_pos(c), first_pos(c + 1)).
   const int per = (S + kThreads - 1) / kThreads;
@@ -148,7 +152,7 @@ paged_decode_kernel(const DecodeArgs a) {
     const int raw = a.seq_lens[s];
     const int L = clamp_len(raw);
     if (raw != L && cta == 0) atomicAdd(a.bad, 1ull);
-    mine += static_cast<long long>(Hkv) * (L + static_cast<long long>(nparts_of(L)) * kUnitCost);
+    mine += static_cast<long long>(NG) * (L + static_cast<long long>(nparts_of(L)) * kUnitCost);
   }
   long long incl = mine;  // inclusive scan within the warp
 #pragma unroll
@@ -182,7 +186,7 @@ paged_decode_kernel(const DecodeArgs a) {
       const int L = clamp_len(a.seq_lens[s]);
       const int np = nparts_of(L);
       const long long w = L + static_cast<long long>(np) * kUnitCost;
-      const long long se = sb + Hkv * w;
+      const long long se = sb + NG * w;
       if (tau <= sb) {
         rs = s; rh = 0; rp = 0; rbase = sb;
         break;
@@ -195,7 +199,7 @@ paged_decode_kernel(const DecodeArgs a) {
           p = 0;
           ++h;
         }
-        if (h >= Hkv) {
+        if (h >= NG) {
           rs = s + 1; rh = 0; rp = 0; rbase = se;
         } else {
           rs = s; rh = h; rp = static_cast<int>(p); rbase = sb;
@@ -210,9 +214,9 @@ paged_decode_kernel(const DecodeArgs a) {
     sW[1 + which] = rbase;
   }
   __syncthreads();
-  const long long Rb = static_cast<long long>(sRange[0]) * Hkv + sRange[1];
+  const long long Rb = static_cast<long long>(sRange[0]) * NG + sRange[1];
   const int pb = sRange[2];
-  const long long Re = static_cast<long long>(sRange[3]) * Hkv + sRange[4];
+  const long long Re = static_cast<long long>(sRange[3]) * NG + sRange[4];
   const int pe = sRange[5];
   if (Rb == Re && pb == pe) return;  // this CTA owns no partition
   const long long nseg_total = (Re - Rb) + (pe > 0 ? 1 : 0);
@@ -225,46 +229,40 @@ paged_decode_kernel(const DecodeArgs a) {
   const int cc = lane % kChunks;  // this lane's 16-byte chunk of a row
   const int cr = lane / kChunks;  // this lane's first row of a tile
   const float sl2 = a.scale_log2;
-  const int tq = 2 * (lane & 3);  // first token column this lane holds in an 8-token n-tile
+  const int r8 = lane >> 2;       // fragment row this lane holds (token of a score tile, dim of an output tile)
+  const int tq = 2 * (lane & 3);  // first fragment column this lane holds (query head)
   const int P = a.max_partitions;
 
-  uint32_t qa[kKSteps][4];
-  float m0, m1, l0, l1;
-  float o[kNTiles][4];
+  // q as the B operand of the score product (B[d][head] = q[head][d]), the
+  // running max / sum of the heads this lane holds (nt*8 + tq, +1), and the
+  // output accumulator O^T[d][head] as MT tiles of 16 dims x 8*NT heads
+  uint32_t qb[kKSteps][NT][2];
+  float mrun[NT][2], lrun[NT][2];
+  float o[kMT][NT][4];
   auto reset_state = [&]() {
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
 #pragma unroll
-    for (int n = 0; n < kNTiles; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) {
+      mrun[nt][0] = mrun[nt][1] = -INFINITY;
+      lrun[nt][0] = lrun[nt][1] = 0.f;
+    }
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
   };
-  auto load_qa = [&]() {
-    const int mi = lane >> 3, rr = lane & 7;
-    const int row = rr + ((mi & 1) << 3);
+  auto load_q = [&](const Seg& g) {
+    const T* qh = static_cast<const T*>(a.query) +
+                  (static_cast<size_t>(g.s) * a.num_q_heads +
+                   static_cast<size_t>(g.hg * Hc + hi) * G) * D;
 #pragma unroll
     for (int kk = 0; kk < kKSteps; ++kk) {
-      const int c = 2 * kk + (mi >> 1);
-      ldmatrix_x4(qa[kk], smem_u32(sQ + row * kRowBytes + swz(row, c)));
-    }
-  };
-  // q rows of a segment, as this thread's share of 16-byte chunks (zero rows >= G)
-  uint4 qreg[Geo::kQRegs];
-  auto fetch_q = [&](const Seg& g) {
-    const T* qg = static_cast<const T*>(a.query) +
-                  (static_cast<size_t>(g.s) * a.num_q_heads + static_cast<size_t>(g.h) * G) * D;
 #pragma unroll
-    for (int k = 0; k < Geo::kQRegs; ++k) {
-      const int i = tid + k * kThreads;
-      const int r = i / kChunks, c = i % kChunks;
-      qreg[k] = r < G ? *reinterpret_cast<const uint4*>(qg + r * D + c * 8)
-                      : make_uint4(0u, 0u, 0u, 0u);
-    }
-  };
-  auto store_q = [&]() {
-#pragma unroll
-    for (int k = 0; k < Geo::kQRegs; ++k) {
-      const int i = tid + k * kThreads;
-      const int r = i / kChunks, c = i % kChunks;
-      *reinterpret_cast<uint4*>(sQ + r * kRowBytes + swz(r, c)) = qreg[k];
+      for (int nt = 0; nt < NT; ++nt) {
+        const int head = nt * 8 + r8;
+        const T* qr = qh + head * D + kk * 16 + tq;
+        qb[kk][nt][0] = head < G ? *reinterpret_cast<const uint32_t*>(qr) : 0u;
+        qb[kk][nt][1] = head < G ? *reinterpret_cast<const uint32_t*>(qr + 8) : 0u;
+      }
     }
   };
 
@@ -273,14 +271,14 @@ paged_decode_kernel(const DecodeArgs a) {
     // ---- segment records of this batch -------------------------------------
     if (tid < nseg) {
       const long long R = Rb + b0 + tid;
-      const int s = static_cast<int>(R / Hkv), h = static_cast<int>(R % Hkv);
+      const int s = static_cast<int>(R / NG), hg = static_cast<int>(R % NG);
       const int L = clamp_len(a.seq_lens[s]);
       const int np = nparts_of(L);
       const int pf = R == Rb ? pb : 0;
       const int pl = R == Re ? pe : np;
       Seg g;
       g.s = s;
-      g.h = h;
+      g.hg = hg;
       g.t0 = pf * Pt;
       g.t1 = static_cast<int>(min(static_cast<long long>(pl) * Pt, static_cast<long long>(L)));
       g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
@@ -309,21 +307,16 @@ paged_decode_kernel(const DecodeArgs a) {
       sSeg[tid] = g;
     }
     __syncthreads();
-    // q of the first segment
-    fetch_q(sSeg[0]);
-    store_q();
-    __syncthreads();
-    load_qa();
+    load_q(sSeg[0]);
     reset_state();
-    if (nseg > 1) fetch_q(sSeg[1]);
 
     // ---- tile iterators over this warp's tiles of the batch ------------------
-    // (segment, tile j): the warp's tiles are j = warp, warp + 4, ... of each segment
+    // (segment, tile j): the warp's tiles are j = ws, ws + Wh, ... of each segment
     auto advance = [&](int& sg, int& j) {
-      j += kWarps;
+      j += Wh;
       while (sg < nseg && j >= sSeg[sg].ntiles) {
         ++sg;
-        j = warp;
+        j = ws;
       }
     };
     // table id of row (lane & 15) of a tile (validated when the copy is issued)
@@ -334,7 +327,7 @@ paged_decode_kernel(const DecodeArgs a) {
       if (t >= g.t1) return 0;
       return __ldg(a.block_tables + static_cast<size_t>(g.s) * a.max_blocks_per_seq + (t >> shift));
     };
-    int id_sg = 0, id_j = warp - kWarps;
+    int id_sg = 0, id_j = ws - Wh;
     advance(id_sg, id_j);
     int is_sg = id_sg, is_j = id_j;
     int idq[kIdDepth];
@@ -350,8 +343,9 @@ paged_decode_kernel(const DecodeArgs a) {
         const int tb = g.t0 + is_j * kTileTokens;
         unsigned char* sk = wpipe + (issued % STAGES) * Geo::kStageBytes;
         unsigned char* sv = sk + Geo::kTileBytes;
-        const T* kb = kcache + static_cast<size_t>(g.h) * D + cc * 8;
-        const T* vb = vcache + static_cast<size_t>(g.h) * D + cc * 8;
+        const size_t hoff = static_cast<size_t>(g.hg * Hc + hi) * D + cc * 8;
+        const T* kb = kcache + hoff;
+        const T* vb = vcache + hoff;
 #pragma unroll
         for (int i = 0; i < kCopies; ++i) {
           const int r = cr + i * kRowsPerCopy;
@@ -375,239 +369,307 @@ paged_decode_kernel(const DecodeArgs a) {
       cp_async_commit();
     };
 #pragma unroll
-    for (int i = 0; i < STAGES - 1; ++i) issue();
+    for (int i = 0; i < STAGES - 1; ++i) issue();  // the loop issues the STAGES-th ahead
     int consumed = 0;
 
     for (int sg = 0; sg < nseg; ++sg) {
       const Seg g = sSeg[sg];
       // ---- this warp's tiles of the segment --------------------------------
-      for (int j = warp; j < g.ntiles; j += kWarps) {
-        cp_async_wait<STAGES - 2>();
+      for (int j = ws; j < g.ntiles; j += Wh) {
+        // refill the slot the previous tile used before waiting, so STAGES
+        // tiles are in flight while this one lands
         __syncwarp();
         issue();
+        cp_async_wait<STAGES - 1>();
+        __syncwarp();
         const unsigned char* sk = wpipe + (consumed % STAGES) * Geo::kStageBytes;
         const unsigned char* sv = sk + Geo::kTileBytes;
         ++consumed;
         const int valid = g.t1 - (g.t0 + j * kTileTokens);  // >= 1
 
-        // scores: [16 rows] x [16 tokens] as two m16n8 tiles
-        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-          const int mi = lane >> 3, rr = lane & 7;
-          const int tok = rr + ((mi >> 1) << 3);
+        // scores S^T[token][head] = K q^T: 16 tokens x 8*NT heads. The k-steps
+        // alternate between two accumulators to halve the dependent chain.
+        float sc[NT][2][4];
 #pragma unroll
-          for (int kk = 0; kk < kKSteps; ++kk) {
-            uint32_t b[4];
-            ldmatrix_x4(b, smem_u32(sk + tok * kRowBytes + swz(tok, 2 * kk + (mi & 1))));
-            Ty::mma(sa, qa[kk], b[0], b[1]);
-            Ty::mma(sb, qa[kk], b[2], b[3]);
-          }
-        }
-        // x[0..3]: row lane/4, tokens tq, tq+1, tq+8, tq+9; x[4..7]: row lane/4+8
-        float x[8] = {sa[0] * sl2, sa[1] * sl2, sb[0] * sl2, sb[1] * sl2,
-                      sa[2] * sl2, sa[3] * sl2, sb[2] * sl2, sb[3] * sl2};
-        if (valid < kTileTokens) {
-          const int tk[4] = {tq, tq + 1, tq + 8, tq + 9};
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (tk[e] >= valid) x[e] = x[e + 4] = -INFINITY;
-          }
-        }
-        float mx0 = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
-        float mx1 = fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7]));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        // weights as A fragments: rows lane/4 (pa[0], pa[2]) and lane/4 + 8
-        // (pa[1], pa[3]); each is a 16-bit head (pa) plus the 16-bit rounding of
-        // the remainder (pl), so the weights keep about 16 significant bits
-        float p[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          p[e] = ex2(x[e] - n0);
-          p[e + 4] = ex2(x[e + 4] - n1);
-        }
-        uint32_t pa[4], pl[4];
-        pa[0] = Ty::pack(p[0], p[1]);
-        pa[1] = Ty::pack(p[4], p[5]);
-        pa[2] = Ty::pack(p[2], p[3]);
-        pa[3] = Ty::pack(p[6], p[7]);
-        {
-          const int src[4][2] = {{0, 1}, {4, 5}, {2, 3}, {6, 7}};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 hd = Ty::unpack(pa[e]);
-            pl[e] = Ty::pack(p[src[e][0]] - hd.x, p[src[e][1]] - hd.y);
-          }
-        }
-        l0 = l0 * al0 + ((p[0] + p[1]) + (p[2] + p[3]));
-        l1 = l1 * al1 + ((p[4] + p[5]) + (p[6] + p[7]));
-        if (__any_sync(kFull, (al0 != 1.f) | (al1 != 1.f))) {
-#pragma unroll
-          for (int n = 0; n < kNTiles; ++n) {
-            o[n][0] *= al0;
-            o[n][1] *= al0;
-            o[n][2] *= al1;
-            o[n][3] *= al1;
-          }
-        }
-        // O += P V: V rows are the k dimension, read transposed
+          for (int e = 0; e < 4; ++e) sc[nt][0][e] = sc[nt][1][e] = 0.f;
         {
           const int mi = lane >> 3, rr = lane & 7;
           const int tok = rr + ((mi & 1) << 3);
 #pragma unroll
-          for (int jj = 0; jj < kNTiles / 2; ++jj) {
-            uint32_t b[4];
-            ldmatrix_x4_trans(b, smem_u32(sv + tok * kRowBytes + swz(tok, 2 * jj + (mi >> 1))));
-            Ty::mma(o[2 * jj], pa, b[0], b[1]);
-            Ty::mma(o[2 * jj + 1], pa, b[2], b[3]);
-            Ty::mma(o[2 * jj], pl, b[0], b[1]);
-            Ty::mma(o[2 * jj + 1], pl, b[2], b[3]);
+          for (int kk = 0; kk < kKSteps; ++kk) {
+            uint32_t ka[4];
+            ldmatrix_x4(ka, smem_u32(sk + tok * kRowBytes + swz(tok, 2 * kk + (mi >> 1))));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) Ty::mma(sc[nt][kk & 1], ka, qb[kk][nt][0], qb[kk][nt][1]);
+          }
+        }
+        // per head (column): lane holds tokens r8 and r8 + 8 for heads nt*8 + tq, +1
+        const bool lo_ok = r8 < valid, hi_ok = r8 + 8 < valid;
+        uint32_t ph[NT][2], pl[NT][2];  // weights as B fragments: 16-bit head, 16-bit remainder
+        float al[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float x[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) x[e] = (sc[nt][0][e] + sc[nt][1][e]) * sl2;
+          if (!lo_ok) x[0] = x[1] = -INFINITY;
+          if (!hi_ok) x[2] = x[3] = -INFINITY;
+          float mx[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(kFull, mx[c], 4));
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(kFull, mx[c], 8));
+            mx[c] = fmaxf(mx[c], __shfl_xor_sync(kFull, mx[c], 16));
+            const float mn = fmaxf(mrun[nt][c], mx[c]);
+            al[nt][c] = ex2(mrun[nt][c] - mn);
+            mrun[nt][c] = mn;
+          }
+          float p[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) p[e] = ex2(x[e] - mrun[nt][e & 1]);
+          lrun[nt][0] = lrun[nt][0] * al[nt][0] + (p[0] + p[2]);
+          lrun[nt][1] = lrun[nt][1] * al[nt][1] + (p[1] + p[3]);
+          // C-fragment pairs (token row, two heads) transposed into B-fragment
+          // pairs (head row, two tokens): tokens 0-7 and 8-15
+          const uint32_t h0 = Ty::pack(p[0], p[1]), h1 = Ty::pack(p[2], p[3]);
+          const float2 d0 = Ty::unpack(h0), d1 = Ty::unpack(h1);
+          const uint32_t r0v = Ty::pack(p[0] - d0.x, p[1] - d0.y);
+          const uint32_t r1v = Ty::pack(p[2] - d1.x, p[3] - d1.y);
+          ph[nt][0] = movmatrix_trans(h0);
+          ph[nt][1] = movmatrix_trans(h1);
+          pl[nt][0] = movmatrix_trans(r0v);
+          pl[nt][1] = movmatrix_trans(r1v);
+        }
+        bool rescale = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) rescale |= (al[nt][0] != 1.f) | (al[nt][1] != 1.f);
+        if (__any_sync(kFull, rescale)) {
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              o[mt][nt][0] *= al[nt][0];
+              o[mt][nt][1] *= al[nt][1];
+              o[mt][nt][2] *= al[nt][0];
+              o[mt][nt][3] *= al[nt][1];
+            }
+        }
+        // O^T[d][head] += V^T P^T: A = V^T read transposed from the [token][d] tile
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int tok = rr + ((mi >> 1) << 3);
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt) {
+            uint32_t va[4];
+            ldmatrix_x4_trans(va, smem_u32(sv + tok * kRowBytes + swz(tok, 2 * mt + (mi & 1))));
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              Ty::mma(o[mt][nt], va, ph[nt][0], ph[nt][1]);
+              Ty::mma(o[mt][nt], va, pl[nt][0], pl[nt][1]);
+            }
           }
         }
       }
 
-      // ---- segment end: merge the four warps (log-sum-exp) --------------------
-      l0 += __shfl_xor_sync(kFull, l0, 1);
-      l1 += __shfl_xor_sync(kFull, l1, 1);
-      l0 += __shfl_xor_sync(kFull, l0, 2);
-      l1 += __shfl_xor_sync(kFull, l1, 2);
-      {
-        float* sMw = sMerge + warp * G * kOS;
-        const int r0 = lane >> 2;
-        if (r0 < G) {
+      // ---- segment end --------------------------------------------------------
+      // full per-head sums: add the partial sums of the 8 lanes holding the same heads
 #pragma unroll
-          for (int n = 0; n < kNTiles; ++n)
-            *reinterpret_cast<float2*>(sMw + r0 * kOS + n * 8 + tq) = make_float2(o[n][0], o[n][1]);
-        }
-        if (r0 + 8 < G) {
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int n = 0; n < kNTiles; ++n)
-            *reinterpret_cast<float2*>(sMw + (r0 + 8) * kOS + n * 8 + tq) =
-                make_float2(o[n][2], o[n][3]);
+        for (int c = 0; c < 2; ++c) {
+          lrun[nt][c] += __shfl_xor_sync(kFull, lrun[nt][c], 4);
+          lrun[nt][c] += __shfl_xor_sync(kFull, lrun[nt][c], 8);
+          lrun[nt][c] += __shfl_xor_sync(kFull, lrun[nt][c], 16);
         }
-        if ((lane & 3) == 0) {
-          sML[(warp * 2 + 0) * kRows + r0] = m0;
-          sML[(warp * 2 + 0) * kRows + r0 + 8] = m1;
-          sML[(warp * 2 + 1) * kRows + r0] = l0;
-          sML[(warp * 2 + 1) * kRows + r0 + 8] = l1;
+      if (Wh > 1) {
+        // warps sharing a head: the others hand their state to the head's first warp
+        if (ws != 0) {
+          float* sMw = sMerge + warp * G * kOS;
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + tq + (e & 1), d = mt * 16 + r8 + ((e & 2) << 2);
+                if (head < G) sMw[head * kOS + d] = o[mt][nt][e];
+              }
+          if (r8 == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                sML[(warp * 2 + 0) * kRows + nt * 8 + tq + c] = mrun[nt][c];
+                sML[(warp * 2 + 1) * kRows + nt * 8 + tq + c] = lrun[nt][c];
+              }
+          }
         }
+        __syncthreads();
+        if (ws == 0) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const int head = nt * 8 + tq + c;
+              float M = mrun[nt][c];
+              for (int w = warp + 1; w < warp + Wh; ++w) M = fmaxf(M, sML[(w * 2) * kRows + head]);
+              const float f = M == -INFINITY ? 0.f : ex2(mrun[nt][c] - M);
+              lrun[nt][c] *= f;
+#pragma unroll
+              for (int mt = 0; mt < kMT; ++mt) {
+                o[mt][nt][c] *= f;
+                o[mt][nt][c + 2] *= f;
+              }
+              for (int w = warp + 1; w < warp + Wh; ++w) {
+                const float gw = M == -INFINITY ? 0.f : ex2(sML[(w * 2) * kRows + head] - M);
+                lrun[nt][c] += gw * sML[(w * 2 + 1) * kRows + head];
+                if (head < G) {
+                  const float* sMw = sMerge + w * G * kOS + head * kOS;
+#pragma unroll
+                  for (int mt = 0; mt < kMT; ++mt) {
+                    o[mt][nt][c] += gw * sMw[mt * 16 + r8];
+                    o[mt][nt][c + 2] += gw * sMw[mt * 16 + r8 + 8];
+                  }
+                }
+              }
+              mrun[nt][c] = M;
+            }
+        }
+        __syncthreads();  // the merge area is reused at the next segment end
       }
-      __syncthreads();
-      if (tid < G) {
-        const int r = tid;
-        float M = -INFINITY;
+
+      if (ws == 0) {
+        // finalize this warp's head: query heads nt*8 + tq (+1) of its group (those < G)
+        const int h = g.hg * Hc + hi;
+        const size_t row0 = static_cast<size_t>(g.s) * a.num_q_heads + static_cast<size_t>(h) * G;
+        float inv[NT][2];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sML[(w * 2) * kRows + r]);
-        float tot = 0.f;
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float f = (M == -INFINITY) ? 0.f : ex2(sML[(w * 2) * kRows + r] - M);
-          sFac[w * kRows + r] = f;
-          tot += f * sML[(w * 2 + 1) * kRows + r];
+          for (int c = 0; c < 2; ++c) inv[nt][c] = lrun[nt][c] > 0.f ? 1.f / lrun[nt][c] : 0.f;
+        if (g.piece < 0) {
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + tq + (e & 1), d = mt * 16 + r8 + ((e & 2) << 2);
+                if (head < G) {
+                  const float v = o[mt][nt][e] * inv[nt][e & 1];
+                  const size_t oi = (row0 + head) * D + d;
+                  if (a.out_f32) {
+                    static_cast<float*>(a.out)[oi] = v;
+                  } else {
+                    static_cast<T*>(a.out)[oi] = Ty::cvt(v);
+                  }
+                }
+              }
+        } else {
+          // store this piece; the head's last piece to arrive merges them in order
+#pragma unroll
+          for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int head = nt * 8 + tq + (e & 1), d = mt * 16 + r8 + ((e & 2) << 2);
+                if (head < G) a.ws_out[((row0 + head) * P + g.piece) * D + d] = o[mt][nt][e] * inv[nt][e & 1];
+              }
+          if (r8 == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int head = nt * 8 + tq + c;
+                if (head < G)
+                  a.ws_lse[(row0 + head) * P + g.piece] =
+                      lrun[nt][c] > 0.f ? mrun[nt][c] + __log2f(lrun[nt][c]) : -INFINITY;
+              }
+          }
+          __syncwarp();
+          int* counter = a.ws_count + static_cast<size_t>(g.s) * Hkv + h;
+          int last = 0;
+          if (lane == 0) {
+            __threadfence();
+            last = atomicAdd(counter, 1) == g.npieces - 1;
+            if (last) __threadfence();
+          }
+          last = __shfl_sync(kFull, last, 0);
+          if (last) {
+            // merge the head's pieces: lane handles 4 consecutive columns of a row
+            const int n = g.npieces;
+            constexpr int kC4 = D / 4;
+            for (int e = lane; e < G * kC4; e += 32) {
+              const int gr = e / kC4, c4 = e % kC4;
+              const float* lse = a.ws_lse + (row0 + gr) * P;
+              const float* po = a.ws_out + (row0 + gr) * P * D + c4 * 4;
+              float M = -INFINITY;
+              for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(lse + k));
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              float den = 0.f;
+              int k = 0;
+              for (; k + 4 <= n; k += 4) {
+                float lv[4];
+                float4 ov[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  lv[u] = __ldcg(lse + k + u);
+                  ov[u] = __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k + u) * D));
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const float wgt = M == -INFINITY ? 0.f : ex2(lv[u] - M);
+                  den += wgt;
+                  acc.x += wgt * ov[u].x;
+                  acc.y += wgt * ov[u].y;
+                  acc.z += wgt * ov[u].z;
+                  acc.w += wgt * ov[u].w;
+                }
+              }
+              for (; k < n; ++k) {
+                const float wgt = M == -INFINITY ? 0.f : ex2(__ldcg(lse + k) - M);
+                const float4 ov = __ldcg(reinterpret_cast<const float4*>(po + static_cast<size_t>(k) * D));
+                den += wgt;
+                acc.x += wgt * ov.x;
+                acc.y += wgt * ov.y;
+                acc.z += wgt * ov.z;
+                acc.w += wgt * ov.w;
+              }
+              const float iv = den > 0.f ? 1.f / den : 0.f;
+              const size_t oi = (row0 + gr) * D + c4 * 4;
+              if (a.out_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(a.out) + oi) =
+                    make_float4(acc.x * iv, acc.y * iv, acc.z * iv, acc.w * iv);
+              } else {
+                uint2 pk;
+                pk.x = Ty::pack(acc.x * iv, acc.y * iv);
+                pk.y = Ty::pack(acc.z * iv, acc.w * iv);
+                *reinterpret_cast<uint2*>(static_cast<T*>(a.out) + oi) = pk;
+              }
+            }
+            if (lane == 0) *counter = 0;  // ready for the next call on this workspace
+          }
         }
-        sFac[kWarps * kRows + r] = tot > 0.f ? 1.f / tot : 0.f;
-        sFac[(kWarps + 1) * kRows + r] = tot > 0.f ? M + __log2f(tot) : -INFINITY;
-      }
-      const bool more = sg + 1 < nseg;
-      if (more) store_q();  // q of the next segment (every warp is past its ldmatrix of this one)
-      __syncthreads();
-      if (more) {
-        load_qa();
-        if (sg + 2 < nseg) fetch_q(sSeg[sg + 2]);
       }
       reset_state();
-
-      const size_t row0 = static_cast<size_t>(g.s) * a.num_q_heads + static_cast<size_t>(g.h) * G;
-      auto merged = [&](int gr, int c) {
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += sFac[w * kRows + gr] * sMerge[(w * G + gr) * kOS + c];
-        return v * sFac[kWarps * kRows + gr];
-      };
-      if (g.piece < 0) {
-        for (int i = tid; i < G * (D / 2); i += kThreads) {
-          const int gr = i / (D / 2), c = 2 * (i % (D / 2));
-          const float v0 = merged(gr, c), v1 = merged(gr, c + 1);
-          const size_t oi = (row0 + gr) * D + c;
-          if (a.out_f32) {
-            *reinterpret_cast<float2*>(static_cast<float*>(a.out) + oi) = make_float2(v0, v1);
-          } else {
-            *reinterpret_cast<uint32_t*>(static_cast<T*>(a.out) + oi) = Ty::pack(v0, v1);
-          }
-        }
-      } else {
-        // store this piece; the last of the row's pieces to arrive merges them in order
-        for (int i = tid; i < G * D; i += kThreads) {
-          const int gr = i / D, c = i % D;
-          a.ws_out[((row0 + gr) * P + g.piece) * D + c] = merged(gr, c);
-        }
-        if (tid < G) a.ws_lse[(row0 + tid) * P + g.piece] = sFac[(kWarps + 1) * kRows + tid];
-        __syncthreads();
-        int* counter = a.ws_count + static_cast<size_t>(g.s) * Hkv + g.h;
-        if (tid == 0) {
-          __threadfence();
-          const int prev = atomicAdd(counter, 1);
-          sFlag = prev == g.npieces - 1;
-          if (sFlag) __threadfence();
-        }
-        __syncthreads();
-        if (sFlag) {
-          const int n = g.npieces;
-          for (int i = tid; i < G * D; i += kThreads) {
-            const int gr = i / D, c = i % D;
-            const float* lse = a.ws_lse + (row0 + gr) * P;
-            const float* po = a.ws_out + (row0 + gr) * P * D + c;
-            float M = -INFINITY;
-            for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(lse + k));
-            float num = 0.f, den = 0.f;
-            int k = 0;
-            for (; k + 4 <= n; k += 4) {
-              float lv[4], ov[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                lv[e] = __ldcg(lse + k + e);
-                ov[e] = __ldcg(po + static_cast<size_t>(k + e) * D);
-              }
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float wgt = ex2(lv[e] - M);
-                den += wgt;
-                num += wgt * ov[e];
-              }
-            }
-            for (; k < n; ++k) {
-              const float wgt = ex2(__ldcg(lse + k) - M);
-              den += wgt;
-              num += wgt * __ldcg(po + static_cast<size_t>(k) * D);
-            }
-            const float v = num / den;
-            const size_t oi = (row0 + gr) * D + c;
-            if (a.out_f32) {
-              static_cast<float*>(a.out)[oi] = v;
-            } else {
-              static_cast<T*>(a.out)[oi] = Ty::cvt(v);
-            }
-          }
-          if (tid == 0) *counter = 0;  // ready for the next call on this workspace
-        }
-      }
-      __syncthreads();  // the merge area, factors and flag are reused at the next segment end
+      if (sg + 1 < nseg) load_q(sSeg[sg + 1]);
     }
     cp_async_wait<0>();
+    __syncthreads();  // the segment records are rewritten for the next batch
   }
 }
 
-template <typename Ty, int D, int STAGES>
-cudaError_t plan_typed(int group, int* ctas_per_sm, size_t* smem) {
-  const size_t bytes = static_cast<size_t>(Geometry<D, STAGES>::kFixedBytes) +
-                       static_cast<size_t>(kWarps) * group * Geometry<D, STAGES>::kOStride * 4;
-  auto kern = paged_decode_kernel<Ty, D, STAGES>;
+template <typename Ty, int D, int STAGES, int NT>
+cudaError_t plan_typed(const DecodeArgs& a, int* ctas_per_sm, size_t* smem) {
+  const int warps_per_head = kWarps / a.heads_per_cta;
+  const size_t merge = warps_per_head > 1 ? static_cast<size_t>(kWarps) * a.group *
+                                                Geometry<D, STAGES>::kOStride * 4
+                                          : 0;
+  const size_t bytes = static_cast<size_t>(Geometry<D, STAGES>::kFixedBytes) + merge;
+  auto kern = paged_decode_kernel<Ty, D, STAGES, NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
@@ -619,38 +681,38 @@ cudaError_t plan_typed(int group, int* ctas_per_sm, size_t* smem) {
   return cudaSuccess;
 }
 
-template <typename Ty, int D, int STAGES>
+template <typename Ty, int D, int STAGES, int NT>
 cudaError_t launch_typed(const DecodeArgs& a, long long grid, size_t smem, cudaStream_t stream) {
-  paged_decode_kernel<Ty, D, STAGES><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
+  paged_decode_kernel<Ty, D, STAGES, NT>
+      <<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <typename Ty, int D>
+template <typename Ty, int D, int NT>
 cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
-  // three ring stages when two CTAs still fit on an SM, else two
+  // the ring depth that fits the most CTAs on an SM (three stages on a tie)
   int n3 = 0, n2 = 0;
   size_t m3 = 0, m2 = 0;
-  cudaError_t e = plan_typed<Ty, D, 3>(a.group, &n3, &m3);
+  cudaError_t e = plan_typed<Ty, D, 3, NT>(a, &n3, &m3);
   if (e != cudaSuccess) return e;
-  int stages = 3, per_sm = n3;
-  size_t smem = m3;
-  if (n3 < 2) {
-    e = plan_typed<Ty, D, 2>(a.group, &n2, &m2);
-    if (e != cudaSuccess) return e;
-    if (n2 > n3) {
-      stages = 2;
-      per_sm = n2;
-      smem = m2;
-    }
-  }
+  e = plan_typed<Ty, D, 2, NT>(a, &n2, &m2);
+  if (e != cudaSuccess) return e;
+  const bool three = n3 >= n2;
+  const int per_sm = three ? n3 : n2;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   long long grid = static_cast<long long>(per_sm) * num_sms;
-  const long long units =
-      static_cast<long long>(a.num_seqs) * a.num_kv_heads * a.max_partitions;
+  const long long units = static_cast<long long>(a.num_seqs) *
+                          (a.num_kv_heads / a.heads_per_cta) * a.max_partitions;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  return stages == 3 ? launch_typed<Ty, D, 3>(a, grid, smem, stream)
-                     : launch_typed<Ty, D, 2>(a, grid, smem, stream);
+  return three ? launch_typed<Ty, D, 3, NT>(a, grid, m3, stream)
+               : launch_typed<Ty, D, 2, NT>(a, grid, m2, stream);
+}
+
+template <typename Ty, int D>
+cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
+  return a.group <= 8 ? launch_d<Ty, D, 1>(a, num_sms, stream)
+                      : launch_d<Ty, D, 2>(a, num_sms, stream);
 }
 
 }  // namespace
@@ -658,11 +720,11 @@ cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
 cudaError_t launch_decode(const DecodeArgs& a, int head_dim, bool bf16, int num_sms,
                           cudaStream_t stream) {
   if (bf16) {
-    return head_dim == 64 ? launch_d<BF16, 64>(a, num_sms, stream)
-                          : launch_d<BF16, 128>(a, num_sms, stream);
+    return head_dim == 64 ? launch_g<BF16, 64>(a, num_sms, stream)
+                          : launch_g<BF16, 128>(a, num_sms, stream);
   }
-  return head_dim == 64 ? launch_d<F16, 64>(a, num_sms, stream)
-                        : launch_d<F16, 128>(a, num_sms, stream);
+  return head_dim == 64 ? launch_g<F16, 64>(a, num_sms, stream)
+                        : launch_g<F16, 128>(a, num_sms, stream);
 }
 
 }  // namespace pa

@@ -22,6 +22,7 @@ struct DecodeArgs {
   int num_q_heads;
   int num_kv_heads;
   int group;          // num_q_heads / num_kv_heads
+  int heads_per_cta;  // kv heads one CTA works on together (4, 2 or 1; divides num_kv_heads)
   int block_shift;    // log2(block_size)
   int max_blocks_per_seq;
   int num_blocks;

@@ -39,6 +39,15 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t add
                : "memory");
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one 32-bit pair per lane
+// (lane l holds row l/4, columns 2(l%4) and 2(l%4)+1); returns the same
+// layout of the transposed matrix.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
 // 2^x (PTX ex2.approx; 2^-inf = +0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
