@@ -343,6 +343,9 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
         "data": "synthetic", "config": _config(case, args) | {"partition_tokens": pt or 512},
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        **({"unique_kv_bytes_per_step": case.unique_kv_bytes(),
+            "unique_kv_GBps": round(case.unique_kv_bytes() * K * world / (ms * 1e-3) / 1e9, 2)}
+           if case.name.startswith("shared_prefix") else {}),
         "tokens_per_s": round(case.num_seqs * K * world / (ms * 1e-3), 1),
         "kv_tokens_per_s": round(float(case.seq_lens.sum()) * K * world / (ms * 1e-3), 1),
         "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": round(achieved, 2),

@@ -42,6 +42,8 @@
 // the 8 row addresses of every ldmatrix phase fall in distinct banks.
 #include <cuda_runtime.h>
 #include <limits.h>
+
+#include <atomic>
 #include <math.h>
 
 #include "internal.h"
@@ -134,17 +136,21 @@ paged_decode_kernel(const DecodeArgs a) {
   Seg* sSeg = reinterpret_cast<Seg*>(sML + kWarps * 2 * kRows);
   float* sMerge =  // [warp][G][kOS], present only when warps share a head
       reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sSeg) + Geo::kSegBytes);
-  __shared__ long long sW[3];  // base position of the first / last unit's sequence
-  __shared__ int sRange[6];    // first unit (s, hg, p), end unit (s, hg, p)
+  __shared__ long long sW[3];  // base position of the first / last unit's row
+  __shared__ int sRange[6];    // first unit (hg, s, p), end unit (hg, s, p)
 
   auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > Lmax ? Lmax : L); };
   auto nparts_of = [&](int L) { return L > 0 ? (L + Pt - 1) / Pt : 1; };
 
   // ======================= schedule ========================================
-  // Every CTA computes the same prefix of sequence weights: a sequence of
-  // length L has ceil(L / Pt) partitions per head group (one if L is 0), each
-  // weighing its tokens plus kUnitCost. CTA c owns the partitions whose start
-  // position lies in [first_pos(c), first_pos(c + 1)).
+  // Rows are taken head-group-major: row R = hg * S + s, so the rows of one
+  // head group over all sequences are consecutive and sequences that share
+  // prefix blocks (consecutive in the batch) re-read them back to back, from
+  // L2. A sequence of length L has ceil(L / Pt) partitions per row (one if L
+  // is 0), each weighing its tokens plus kUnitCost; every CTA computes the
+  // same prefix of these weights over the sequences (one pass, Wseq), and the
+  // positions of head group hg are offset by hg * Wseq. CTA c owns the
+  // partitions whose start position lies in [first_pos(c), first_pos(c + 1)).
   const int per = (S + kThreads - 1) / kThreads;
   const int s_lo = min(S, tid * per), s_hi = min(S, s_lo + per);
   long long mine = 0;
@@ -152,7 +158,7 @@ paged_decode_kernel(const DecodeArgs a) {
     const int raw = a.seq_lens[s];
     const int L = clamp_len(raw);
     if (raw != L && cta == 0) atomicAdd(a.bad, 1ull);
-    mine += static_cast<long long>(NG) * (L + static_cast<long long>(nparts_of(L)) * kUnitCost);
+    mine += L + static_cast<long long>(nparts_of(L)) * kUnitCost;
   }
   long long incl = mine;  // inclusive scan within the warp
 #pragma unroll
@@ -163,60 +169,59 @@ paged_decode_kernel(const DecodeArgs a) {
   long long* sScan = reinterpret_cast<long long*>(sPipe);
   if (lane == 31) sScan[warp] = incl;
   if (tid == 0) {
-    sRange[0] = S; sRange[1] = 0; sRange[2] = 0;
-    sRange[3] = S; sRange[4] = 0; sRange[5] = 0;
+    sRange[0] = NG; sRange[1] = 0; sRange[2] = 0;
+    sRange[3] = NG; sRange[4] = 0; sRange[5] = 0;
+    sW[1] = sW[2] = 0;
   }
   __syncthreads();
   long long base = incl - mine;
   for (int w = 0; w < warp; ++w) base += sScan[w];
-  long long Wtot = 0;
-  for (int w = 0; w < kWarps; ++w) Wtot += sScan[w];
+  long long Wseq = 0;
+  for (int w = 0; w < kWarps; ++w) Wseq += sScan[w];
+  const long long Wtot = Wseq * NG;
   const long long tau_b = first_pos(cta, C, Wtot);
   const long long tau_e = first_pos(cta + 1, C, Wtot);
   // the first partition at or after position tau, found by the thread whose
-  // chunk of sequences holds tau
+  // chunk of sequences holds tau's offset within its head group
   for (int which = 0; which < 2; ++which) {
     const long long tau = which == 0 ? tau_b : tau_e;
-    const bool claim = (tid == 0 && tau <= 0) || (mine > 0 && base < tau && tau <= base + mine);
+    if (tau >= Wtot) continue;  // past the last partition: the default (NG, 0, 0)
+    const int hg = static_cast<int>(tau / Wseq);
+    const long long off = tau - hg * Wseq;
+    const bool claim = (tid == 0 && off <= 0) || (mine > 0 && base < off && off <= base + mine);
     if (!claim) continue;
     long long sb = base;
-    int rs = s_hi, rh = 0, rp = 0;
+    int rs = s_hi, rp = 0;
     long long rbase = base + mine;
     for (int s = s_lo; s < s_hi; ++s) {
       const int L = clamp_len(a.seq_lens[s]);
       const int np = nparts_of(L);
-      const long long w = L + static_cast<long long>(np) * kUnitCost;
-      const long long se = sb + NG * w;
-      if (tau <= sb) {
-        rs = s; rh = 0; rp = 0; rbase = sb;
+      const long long se = sb + L + static_cast<long long>(np) * kUnitCost;
+      if (off <= sb) {
+        rs = s; rp = 0; rbase = sb;
         break;
       }
-      if (tau < se) {
-        const long long r = tau - sb;
-        int h = static_cast<int>(r / w);
-        long long p = (r - h * w + UW - 1) / UW;
+      if (off < se) {
+        const long long p = (off - sb + UW - 1) / UW;
         if (p >= np) {
-          p = 0;
-          ++h;
-        }
-        if (h >= NG) {
-          rs = s + 1; rh = 0; rp = 0; rbase = se;
+          rs = s + 1; rp = 0; rbase = se;
         } else {
-          rs = s; rh = h; rp = static_cast<int>(p); rbase = sb;
+          rs = s; rp = static_cast<int>(p); rbase = sb;
         }
         break;
       }
       sb = se;
     }
-    sRange[which * 3 + 0] = rs;
-    sRange[which * 3 + 1] = rh;
+    // (hg, S) is the first row of the next head group
+    sRange[which * 3 + 0] = hg;
+    sRange[which * 3 + 1] = rs;
     sRange[which * 3 + 2] = rp;
-    sW[1 + which] = rbase;
+    sW[1 + which] = static_cast<long long>(hg) * Wseq + rbase;  // the row's base position
   }
   __syncthreads();
-  const long long Rb = static_cast<long long>(sRange[0]) * NG + sRange[1];
+  const long long Rb = static_cast<long long>(sRange[0]) * S + sRange[1];
   const int pb = sRange[2];
-  const long long Re = static_cast<long long>(sRange[3]) * NG + sRange[4];
+  const long long Re = static_cast<long long>(sRange[3]) * S + sRange[4];
   const int pe = sRange[5];
   if (Rb == Re && pb == pe) return;  // this CTA owns no partition
   const long long nseg_total = (Re - Rb) + (pe > 0 ? 1 : 0);
@@ -271,7 +276,7 @@ paged_decode_kernel(const DecodeArgs a) {
     // ---- segment records of this batch -------------------------------------
     if (tid < nseg) {
       const long long R = Rb + b0 + tid;
-      const int s = static_cast<int>(R / NG), hg = static_cast<int>(R % NG);
+      const int hg = static_cast<int>(R / S), s = static_cast<int>(R % S);
       const int L = clamp_len(a.seq_lens[s]);
       const int np = nparts_of(L);
       const int pf = R == Rb ? pb : 0;
@@ -288,9 +293,7 @@ paged_decode_kernel(const DecodeArgs a) {
       if (!(pf == 0 && pl == np)) {
         // a row cut between CTAs: walk its owners in order to find this CTA's
         // piece index and the number of pieces
-        const long long w = L + static_cast<long long>(np) * kUnitCost;
-        const long long rowbase = R == Rb ? sW[1] + static_cast<long long>(sRange[1]) * w
-                                          : sW[2] + static_cast<long long>(sRange[4]) * w;
+        const long long rowbase = R == Rb ? sW[1] : sW[2];
         int c = owner_of(rowbase, C, Wtot);
         int k = 0, me = -1;
         while (true) {
@@ -669,9 +672,13 @@ cudaError_t plan_typed(const DecodeArgs& a, int* ctas_per_sm, size_t* smem) {
                                                 Geometry<D, STAGES>::kOStride * 4
                                           : 0;
   const size_t bytes = static_cast<size_t>(Geometry<D, STAGES>::kFixedBytes) + merge;
+  // the attribute is an upper bound shared by every call of this kernel: set it
+  // to the largest request (a full merge area for 16 query heads)
+  const size_t most = static_cast<size_t>(Geometry<D, STAGES>::kFixedBytes) +
+                      static_cast<size_t>(kWarps) * kMaxGroup * Geometry<D, STAGES>::kOStride * 4;
   auto kern = paged_decode_kernel<Ty, D, STAGES, NT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(bytes));
+                                       static_cast<int>(most));
   if (e != cudaSuccess) return e;
   int n = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, bytes);
@@ -688,25 +695,46 @@ cudaError_t launch_typed(const DecodeArgs& a, long long grid, size_t smem, cudaS
   return cudaGetLastError();
 }
 
+// Launch plans (ring depth, CTAs per SM, shared memory) cached per device
+// and kernel variant, so the occupancy query runs once, not on every call.
+constexpr int kPlanDevices = 64;
+constexpr int kPlanSlots = 2 * 2 * 2 * (kMaxGroup + 1) * 3;
+std::atomic<unsigned long long> g_plans[kPlanDevices][kPlanSlots];
+
 template <typename Ty, int D, int NT>
 cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
-  // the ring depth that fits the most CTAs on an SM (three stages on a tie)
-  int n3 = 0, n2 = 0;
-  size_t m3 = 0, m2 = 0;
-  cudaError_t e = plan_typed<Ty, D, 3, NT>(a, &n3, &m3);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = plan_typed<Ty, D, 2, NT>(a, &n2, &m2);
-  if (e != cudaSuccess) return e;
-  const bool three = n3 >= n2;
-  const int per_sm = three ? n3 : n2;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int hc_slot = a.heads_per_cta == 4 ? 2 : (a.heads_per_cta == 2 ? 1 : 0);
+  const int slot = (((Ty::kIsBf16 ? 1 : 0) * 2 + (D == 128 ? 1 : 0)) * 2 +
+                    (NT - 1)) * (kMaxGroup + 1) * 3 + a.group * 3 + hc_slot;
+  unsigned long long plan = (dev >= 0 && dev < kPlanDevices) ? g_plans[dev][slot].load() : 0ull;
+  if (plan == 0) {
+    // the ring depth that fits the most CTAs on an SM (three stages on a tie)
+    int n3 = 0, n2 = 0;
+    size_t m3 = 0, m2 = 0;
+    e = plan_typed<Ty, D, 3, NT>(a, &n3, &m3);
+    if (e != cudaSuccess) return e;
+    e = plan_typed<Ty, D, 2, NT>(a, &n2, &m2);
+    if (e != cudaSuccess) return e;
+    const bool three = n3 >= n2;
+    const unsigned long long per = static_cast<unsigned long long>(three ? n3 : n2);
+    const unsigned long long mem = three ? m3 : m2;
+    if (per < 1) return cudaErrorInvalidConfiguration;
+    plan = (three ? 1ull : 2ull) | (per << 2) | (mem << 16);
+    if (dev >= 0 && dev < kPlanDevices) g_plans[dev][slot].store(plan);
+  }
+  const bool three = (plan & 3ull) == 1ull;
+  const int per_sm = static_cast<int>((plan >> 2) & 0x3fffull);
+  const size_t smem = static_cast<size_t>(plan >> 16);
   long long grid = static_cast<long long>(per_sm) * num_sms;
   const long long units = static_cast<long long>(a.num_seqs) *
                           (a.num_kv_heads / a.heads_per_cta) * a.max_partitions;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  return three ? launch_typed<Ty, D, 3, NT>(a, grid, m3, stream)
-               : launch_typed<Ty, D, 2, NT>(a, grid, m2, stream);
+  return three ? launch_typed<Ty, D, 3, NT>(a, grid, smem, stream)
+               : launch_typed<Ty, D, 2, NT>(a, grid, smem, stream);
 }
 
 template <typename Ty, int D>

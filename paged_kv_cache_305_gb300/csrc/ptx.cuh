@@ -59,6 +59,7 @@ __device__ __forceinline__ float ex2(float x) {
 // nearest even) and the m16n8k16 tensor-core product with fp32 accumulation.
 struct F16 {
   using T = __half;
+  static constexpr bool kIsBf16 = false;
   __device__ __forceinline__ static T cvt(float v) { return __float2half_rn(v); }
   __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
@@ -79,6 +80,7 @@ struct F16 {
 
 struct BF16 {
   using T = __nv_bfloat16;
+  static constexpr bool kIsBf16 = true;
   __device__ __forceinline__ static T cvt(float v) { return __float2bfloat16_rn(v); }
   __device__ __forceinline__ static uint32_t pack(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
