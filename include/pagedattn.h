@@ -51,7 +51,8 @@ enum {
   PA_ERR_INVALID = -1,     /* a null pointer, a bad size or a misaligned pointer */
   PA_ERR_UNSUPPORTED = -2, /* valid, but outside what the kernels are built for */
   PA_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
-  PA_ERR_CUDA = -4         /* a CUDA call failed; the message names it */
+  PA_ERR_CUDA = -4,        /* a CUDA call failed; the message names it */
+  PA_ERR_CAPACITY = -5     /* the block pool or a block table is full (nothing changed) */
 };
 
 /*
@@ -177,6 +178,74 @@ int pa_decode_no_alloc(void* out, const void* query,
 
 /* Size in bytes of the fixed scratch that pa_decode_no_alloc uses. */
 size_t pa_decode_no_alloc_scratch_bytes(void);
+
+/*
+ * Block copies inside the pools, the device half of copy-on-write
+ * ("PagedAttention by hand", Why divide memory into physical blocks?:
+ * allocate a fresh block, copy that one block's contents, write into the
+ * copy). For i < num_copies, the whole block src[i] (B * Hkv * d elements)
+ * of key_cache and of value_cache is copied onto block dst[i].
+ * src, dst: DEVICE int32 arrays of num_copies block ids. A pair with an id
+ * outside [0, num_blocks) is skipped and counted by pa_bad_index_count;
+ * src == dst is a no-op. Copies whose blocks overlap (a dst that is another
+ * pair's src) race. Sizes as for pa_reshape_and_cache.
+ * Errors: PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA.
+ */
+int pa_copy_blocks(void* key_cache, void* value_cache,
+                   const int32_t* src, const int32_t* dst, int num_copies,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   pa_dtype dtype, cudaStream_t stream);
+
+/*
+ * Block manager: host-side bookkeeping of the pool ("PagedAttention by hand",
+ * What is PagedAttention: free blocks are a stack of interchangeable ids, a
+ * block table maps each sequence's logical blocks to physical ones; Why divide
+ * memory into physical blocks?: reference counts and copy-on-write; the
+ * "PagedAttention" glossary: a new block only when the previous one fills).
+ * Every pointer here is HOST memory. Not thread-safe: serialise the calls on
+ * one manager. Free-stack order: block 0 is handed out first on a fresh pool;
+ * a freed sequence pushes its blocks in table order and allocation pops the
+ * most recently pushed. Errors: PA_ERR_INVALID (bad id, NULL, duplicates,
+ * capacities), PA_ERR_CAPACITY (pool or table full; nothing changed).
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager of num_blocks blocks of block_size slots; tables hold at most
+ * max_blocks_per_seq blocks. *out receives the handle. */
+int pa_bm_create(int num_blocks, int block_size, int max_blocks_per_seq, pa_block_manager** out);
+void pa_bm_destroy(pa_block_manager* bm);
+
+/* A new, empty sequence; its id is written to *seq_id (freed ids are reused). */
+int pa_bm_new_sequence(pa_block_manager* bm, int* seq_id);
+
+/* A new sequence sharing all blocks of `parent` (their reference counts + 1),
+ * e.g. one more sample of the same prompt. */
+int pa_bm_fork(pa_block_manager* bm, int parent, int* child);
+
+/* Drops the sequence: blocks whose reference count reaches 0 become free. */
+int pa_bm_free_sequence(pa_block_manager* bm, int seq_id);
+
+/*
+ * Reserves slots for num_new[i] new tokens of sequence seq_ids[i], for
+ * i < count, in order (a sequence appears at most once). Writes the slot of
+ * every new token (block * block_size + offset), in request order, to
+ * slot_mapping (room for slot_capacity entries), and the copy-on-write block
+ * copies the writes need to copy_src / copy_dst (room for copy_capacity >=
+ * count pairs; at most one per sequence), their number to *num_copies. The
+ * caller performs those copies (pa_copy_blocks) before writing the tokens
+ * (pa_reshape_and_cache with this slot_mapping).
+ */
+int pa_bm_append(pa_block_manager* bm, const int* seq_ids, const int* num_new, int count,
+                 int64_t* slot_mapping, int slot_capacity,
+                 int32_t* copy_src, int32_t* copy_dst, int copy_capacity, int* num_copies);
+
+/* Block tables [count, max_blocks_per_seq] (unused entries 0) and lengths
+ * [count] of the listed sequences, ready to upload for pa_decode. */
+int pa_bm_block_tables(const pa_block_manager* bm, const int* seq_ids, int count,
+                       int32_t* block_tables, int32_t* seq_lens);
+
+int pa_bm_num_free_blocks(const pa_block_manager* bm, int* n);
+int pa_bm_ref_count(const pa_block_manager* bm, int block, int* count);
 
 /*
  * Message for the most recent non-OK return on the calling thread ("" if

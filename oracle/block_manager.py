@@ -30,6 +30,8 @@ from __future__ import annotations
 
 from typing import Dict, List, Sequence, Tuple
 
+import numpy as np
+
 
 class CapacityError(RuntimeError):
     pass
@@ -143,3 +145,11 @@ class BlockManager:
             t = self.tables[sid]
             rows.append(t + [0] * (self.max_blocks_per_seq - len(t)))
         return rows, [self.lens[s] for s in sids]
+
+
+def copy_blocks(key_cache: np.ndarray, value_cache: np.ndarray, pairs) -> None:
+    """Copy-on-write's device step: block src's contents onto block dst, in both
+    caches, for each (src, dst) pair, in place."""
+    for src, dst in pairs:
+        key_cache[dst] = key_cache[src]
+        value_cache[dst] = value_cache[src]

@@ -7,9 +7,12 @@ from .pagedattn import (  # noqa: F401
     PA_BFLOAT16,
     PA_FLOAT16,
     PA_FLOAT32,
+    PA_ERR_CAPACITY,
+    BlockManager,
     PagedAttnError,
     alloc_workspace,
     bad_index_count,
+    copy_blocks,
     decode,
     decode_no_alloc,
     decode_workspace_bytes,

@@ -34,7 +34,7 @@ def nvcc_path() -> str:
 
 
 def sources() -> List[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> List[str]:
@@ -60,7 +60,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
     procs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         objs.append(obj)
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         if verbose:

@@ -100,6 +100,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 namespace pa {
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+void clear_error() { g_error.clear(); }
 
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions) {
   WorkspaceLayout w{};
@@ -164,6 +165,34 @@ int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, vo
       key, value, key_cache, value_cache, slot_mapping, num_tokens, static_cast<int>(row_bytes),
       static_cast<long long>(num_blocks) * block_size, bad, stream);
   if (e != cudaSuccess) return cuda_fail(e, "reshape_and_cache launch");
+  return PA_OK;
+}
+
+int pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* src, const int32_t* dst,
+                   int num_copies, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   pa_dtype dtype, cudaStream_t stream) {
+  g_error.clear();
+  int rc = check_dtype(dtype);
+  if (rc != PA_OK) return rc;
+  if (num_copies < 0) return fail(PA_ERR_INVALID, "num_copies %d < 0", num_copies);
+  if (num_kv_heads < 1) return fail(PA_ERR_INVALID, "num_kv_heads %d < 1", num_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (log2_pow2(block_size) < 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two up to 64)", block_size);
+  if (num_blocks < 1) return fail(PA_ERR_INVALID, "num_blocks %d < 1", num_blocks);
+  if (num_copies == 0) return PA_OK;
+  if (!key_cache || !value_cache || !src || !dst) return fail(PA_ERR_INVALID, "a pointer argument is NULL");
+  if (!aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID, "the caches must be 16-byte aligned");
+  if (!aligned4(src) || !aligned4(dst)) return fail(PA_ERR_INVALID, "src and dst must be 4-byte aligned");
+  unsigned long long* bad = nullptr;
+  rc = bad_counter(&bad);
+  if (rc != PA_OK) return rc;
+  const long long block_bytes = static_cast<long long>(block_size) * num_kv_heads * head_dim * 2;
+  cudaError_t e = pa::launch_copy_blocks(key_cache, value_cache, src, dst, num_copies, block_bytes,
+                                         num_blocks, bad, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
   return PA_OK;
 }
 

@@ -36,8 +36,10 @@ struct DecodeArgs {
   unsigned long long* bad;  // device counter of rejected indices
 };
 
-// Records `msg` as the calling thread's last error and returns `code`.
+// Records `msg` as the calling thread's last error and returns `code`;
+// clear_error() empties it (entry points call it first).
 int set_error(int code, const char* msg);
+void clear_error();
 
 // Workspace carve-up shared by pa_decode_workspace_bytes and pa_decode.
 struct WorkspaceLayout {
@@ -55,6 +57,10 @@ constexpr int kMaxSegments = 64;
 // multiple of it).
 cudaError_t launch_decode(const DecodeArgs& a, int head_dim, bool bf16, int num_sms,
                           cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* key_cache, void* value_cache, const int32_t* src,
+                               const int32_t* dst, int num_copies, long long block_bytes,
+                               int num_blocks, unsigned long long* bad, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* key, const void* value, void* key_cache,
                                      void* value_cache, const int64_t* slot_mapping,

@@ -21,7 +21,10 @@ PA_FLOAT16, PA_BFLOAT16, PA_FLOAT32 = 0, 1, 2
 _DTYPES = {torch.float16: PA_FLOAT16, torch.bfloat16: PA_BFLOAT16}
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_last_error", "pa_bad_index_count", "pa_decode_no_alloc",
-            "pa_decode_no_alloc_scratch_bytes")
+            "pa_decode_no_alloc_scratch_bytes", "pa_copy_blocks", "pa_bm_create",
+            "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
+            "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count")
+PA_ERR_CAPACITY = -5
 
 _lib = None
 
@@ -59,6 +62,27 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_no_alloc.restype = i32
     L.pa_decode_no_alloc_scratch_bytes.argtypes = []
     L.pa_decode_no_alloc_scratch_bytes.restype = sz
+    L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    L.pa_copy_blocks.restype = i32
+    ip = ctypes.POINTER(ctypes.c_int)
+    L.pa_bm_create.argtypes = [i32, i32, i32, ctypes.POINTER(vp)]
+    L.pa_bm_create.restype = i32
+    L.pa_bm_destroy.argtypes = [vp]
+    L.pa_bm_destroy.restype = None
+    L.pa_bm_new_sequence.argtypes = [vp, ip]
+    L.pa_bm_new_sequence.restype = i32
+    L.pa_bm_fork.argtypes = [vp, i32, ip]
+    L.pa_bm_fork.restype = i32
+    L.pa_bm_free_sequence.argtypes = [vp, i32]
+    L.pa_bm_free_sequence.restype = i32
+    L.pa_bm_append.argtypes = [vp, vp, vp, i32, vp, i32, vp, vp, i32, ip]
+    L.pa_bm_append.restype = i32
+    L.pa_bm_block_tables.argtypes = [vp, vp, i32, vp, vp]
+    L.pa_bm_block_tables.restype = i32
+    L.pa_bm_num_free_blocks.argtypes = [vp, ip]
+    L.pa_bm_num_free_blocks.restype = i32
+    L.pa_bm_ref_count.argtypes = [vp, i32, ip]
+    L.pa_bm_ref_count.restype = i32
     _lib = L
     return L
 
@@ -213,3 +237,92 @@ def decode_no_alloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
 def no_alloc_scratch_bytes() -> int:
     """Bytes of the fixed split-K scratch behind :func:`decode_no_alloc`."""
     return int(load_library().pa_decode_no_alloc_scratch_bytes())
+
+
+def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, src: torch.Tensor,
+                dst: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks src[i] -> dst[i] (int32 CUDA tensors) in both caches."""
+    _need(key_cache.is_cuda and key_cache.is_contiguous() and value_cache.is_contiguous(),
+          "caches must be contiguous CUDA tensors")
+    _need(src.dtype == torch.int32 and dst.dtype == torch.int32 and src.shape == dst.shape
+          and src.dim() == 1 and src.is_cuda and dst.is_cuda, "src/dst must be 1-D int32 CUDA tensors")
+    NB, B, Hkv, d = key_cache.shape
+    L = load_library()
+    with torch.cuda.device(key_cache.device):
+        _check(L.pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src.data_ptr(),
+                                dst.data_ptr(), src.numel(), Hkv, d, B, NB, _dtype_code(key_cache),
+                                _stream(key_cache, stream)))
+
+
+class BlockManager:
+    """The library's native block manager (host memory; see include/pagedattn.h)."""
+
+    def __init__(self, num_blocks: int, block_size: int, max_blocks_per_seq: int):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check(self._lib.pa_bm_create(num_blocks, block_size, max_blocks_per_seq, ctypes.byref(h)))
+        self._h = h
+        self.block_size = block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_sequence(self) -> int:
+        out = ctypes.c_int()
+        _check(self._lib.pa_bm_new_sequence(self._h, ctypes.byref(out)))
+        return out.value
+
+    def fork(self, parent: int) -> int:
+        out = ctypes.c_int()
+        _check(self._lib.pa_bm_fork(self._h, parent, ctypes.byref(out)))
+        return out.value
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(self._lib.pa_bm_free_sequence(self._h, seq_id))
+
+    def append(self, requests):
+        """Slots for new tokens of (seq_id, count) requests and the copy-on-write copies.
+
+        Returns (slot_mapping int64 array, [(src, dst), ...]).
+        """
+        import numpy as np
+        ids = np.array([r[0] for r in requests], dtype=np.int32)
+        num = np.array([r[1] for r in requests], dtype=np.int32)
+        total = int(num.sum()) if len(num) else 0
+        slots = np.zeros(max(total, 1), dtype=np.int64)
+        csrc = np.zeros(max(len(ids), 1), dtype=np.int32)
+        cdst = np.zeros(max(len(ids), 1), dtype=np.int32)
+        nc = ctypes.c_int()
+        _check(self._lib.pa_bm_append(self._h, ids.ctypes.data, num.ctypes.data, len(ids),
+                                      slots.ctypes.data, total, csrc.ctypes.data, cdst.ctypes.data,
+                                      len(ids), ctypes.byref(nc)))
+        return slots[:total], [(int(csrc[i]), int(cdst[i])) for i in range(nc.value)]
+
+    def block_tables(self, seq_ids):
+        """(int32 [len, max_blocks_per_seq] tables, int32 [len] lengths) of the sequences."""
+        import numpy as np
+        ids = np.array(seq_ids, dtype=np.int32)
+        tables = np.zeros((len(ids), self.max_blocks_per_seq), dtype=np.int32)
+        lens = np.zeros(len(ids), dtype=np.int32)
+        _check(self._lib.pa_bm_block_tables(self._h, ids.ctypes.data, len(ids), tables.ctypes.data,
+                                            lens.ctypes.data))
+        return tables, lens
+
+    def num_free_blocks(self) -> int:
+        out = ctypes.c_int()
+        _check(self._lib.pa_bm_num_free_blocks(self._h, ctypes.byref(out)))
+        return out.value
+
+    def ref_count(self, block: int) -> int:
+        out = ctypes.c_int()
+        _check(self._lib.pa_bm_ref_count(self._h, block, ctypes.byref(out)))
+        return out.value

@@ -12,9 +12,10 @@
 """
 import random
 
+import numpy as np
 import pytest
 
-from oracle.block_manager import BlockManager, CapacityError
+from oracle.block_manager import BlockManager, CapacityError, copy_blocks
 
 
 def _check_invariants(bm):
@@ -127,3 +128,14 @@ def test_random_operations_keep_the_invariants():
         except CapacityError:
             pass
         _check_invariants(bm)
+
+
+def test_copy_blocks_moves_whole_blocks():
+    kc = np.arange(5 * 2 * 3, dtype=np.uint16).reshape(5, 2, 3)
+    vc = kc + 100
+    k0, v0 = kc.copy(), vc.copy()
+    copy_blocks(kc, vc, [(1, 3), (4, 0)])
+    assert np.array_equal(kc[3], k0[1]) and np.array_equal(vc[3], v0[1])
+    assert np.array_equal(kc[0], k0[4]) and np.array_equal(vc[0], v0[4])
+    for b in (1, 2, 4):
+        assert np.array_equal(kc[b], k0[b]) and np.array_equal(vc[b], v0[b])
