@@ -368,6 +368,159 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# Secondary measurements (one JSON line each; not the headline)
+# ---------------------------------------------------------------------------
+def _events(fn, steps, warmup):
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
+def run_copy_blocks(args):
+    """Block copies (the device half of copy-on-write): GB/s moved, HBM-bound."""
+    import torch
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    NB, B, Hkv, d = 44188, 16, 8, 128  # the GQA workload's pool
+    kc = torch.randn((NB, B, Hkv, d), device="cuda").to(torch.bfloat16)
+    vc = torch.randn_like(kc)
+    n = 4096
+    perm = torch.randperm(NB, device="cuda").to(torch.int32)
+    src, dst = perm[:n].contiguous(), perm[n:2 * n].contiguous()
+    ms = _events(lambda: pa.copy_blocks(kc, vc, src, dst), args.steps, max(3, args.warmup))
+    moved = 2 * 2 * n * B * Hkv * d * 2  # read + write, K and V
+    peak, kind = _peaks()
+    gbs = moved / (ms * 1e-3) / 1e9
+    print(json.dumps({"op": "copy_blocks", "metric": "block copy GB/s (read + write)", "value": round(gbs, 1),
+                      "unit": "GB/s", "frac_of_hbm_peak": round(gbs / peak, 4), "peak_kind": kind,
+                      "ms_per_call": round(ms, 4), "steps": args.steps,
+                      "config": {"copies": n, "block_bytes": B * Hkv * d * 2, "dtype": "bf16"}}))
+
+
+def run_block_manager(args):
+    """Host throughput of the native block manager's append (one token per sequence)."""
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    S, B = 128, 16
+    bm = pa.BlockManager(200000, B, 1024)
+    seqs = []
+    for i in range(S // 4):
+        p = bm.new_sequence()
+        bm.append([(p, 1000 + 37 * i)])
+        seqs.append(p)
+        seqs.extend(bm.fork(p) for _ in range(3))  # 4 candidates share the prompt
+    reqs = [(sq, 1) for sq in seqs]
+    for _ in range(10):
+        bm.append(reqs)
+    n = max(100, args.steps)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        bm.append(reqs)
+    dt = (time.perf_counter() - t0) / n
+    tt = time.perf_counter()
+    for _ in range(n):
+        bm.block_tables(seqs)
+    dtt = (time.perf_counter() - tt) / n
+    print(json.dumps({"op": "block_manager", "metric": "block-manager appends per second (host)",
+                      "value": round(S / dt, 1), "unit": "appends/s", "us_per_append_call": round(dt * 1e6, 2),
+                      "us_per_table_export": round(dtt * 1e6, 2), "calls": n,
+                      "config": {"sequences": S, "block_size": B, "candidates_per_prompt": 4,
+                                 "binding": "ctypes (includes Python marshalling)"}}))
+
+
+def run_serving_step(args):
+    """One serving decode step through the native block manager: append one token
+    per sequence (copy-on-write where candidates diverge), upload slots and
+    tables, copy blocks, write the new K/V, decode."""
+    import torch
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    rng = np.random.default_rng(0)
+    S, Hq, Hkv, d, B = 128, 32, 8, 128, 16
+    prompts = rng.integers(1024, 8193, size=S // 4)
+    NB = int(1.3 * (sum(int(p) // B + 2 for p in prompts) + S * (args.steps + args.warmup + 16) // B + S))
+    MB = 8192 // B + (args.steps + args.warmup) // B + 4
+    bm = pa.BlockManager(NB, B, MB)
+    dt = torch.bfloat16
+    kc = torch.randn((NB, B, Hkv, d), device="cuda").to(dt)
+    vc = torch.randn_like(kc)
+    seqs = []
+    for p in prompts:
+        sid = bm.new_sequence()
+        bm.append([(sid, int(p))])  # prompt K/V: the random pool contents stand in
+        seqs.append(sid)
+        seqs.extend(bm.fork(sid) for _ in range(3))
+    q = torch.randn((S, Hq, d), device="cuda").to(dt)
+    nk = torch.randn((S, Hkv, d), device="cuda").to(dt)
+    nv = torch.randn_like(nk)
+    out = torch.empty_like(q)
+    reqs = [(sq, 1) for sq in seqs]
+    ws = pa.alloc_workspace(q, kc, torch.empty((S, MB), dtype=torch.int32), 0)
+    copies_seen = [0]
+    bytes_seen = [0]
+
+    def step():
+        slots, copies = bm.append(reqs)
+        tables, lens = bm.block_tables(seqs)
+        slots_d = torch.from_numpy(slots).pin_memory().cuda(non_blocking=True)
+        bt = torch.from_numpy(tables).pin_memory().cuda(non_blocking=True)
+        sl = torch.from_numpy(lens).pin_memory().cuda(non_blocking=True)
+        if copies:
+            c = torch.tensor(copies, dtype=torch.int32).t().contiguous().cuda(non_blocking=True)
+            pa.copy_blocks(kc, vc, c[0], c[1])
+            copies_seen[0] += len(copies)
+        pa.reshape_and_cache(nk, nv, kc, vc, slots_d)
+        pa.decode(out, q, kc, vc, bt, sl, None, 0, ws)
+        bytes_seen[0] += int(2 * lens.astype(np.int64).sum() * Hkv * d * 2)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    copies_seen[0], bytes_seen[0] = 0, 0
+    t0 = time.perf_counter()
+    steps = min(args.steps, 200)
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    print(json.dumps({"op": "serving_step", "metric": "serving decode step through the block manager",
+                      "value": round(S * steps / el, 1), "unit": "tokens/s",
+                      "ms_per_step": round(1e3 * el / steps, 4),
+                      "kv_GBps": round(bytes_seen[0] / el / 1e9, 1), "cow_copies": copies_seen[0],
+                      "steps": steps, "timing": "wall clock, host and device",
+                      "config": {"sequences": S, "prompts": S // 4, "candidates_per_prompt": 4,
+                                 "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
+                                 "block_size": B, "prompt_len_range": [1024, 8192], "dtype": "bf16"}}))
+
+
+def run_waste(args):
+    """KV-memory waste of paged vs contiguous reservation on a synthetic trace."""
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    from paged_kv_cache_305_gb300 import waste
+    rows = {}
+    for B in (1, 8, 16, 32, 64):
+        r = waste.simulate(block_size=B)
+        rows[str(B)] = {"paged_waste": round(r.paged_waste, 4), "contiguous_waste": round(r.contiguous_waste, 4),
+                        "max_paged_waste_per_seq": r.max_paged_waste_per_seq}
+    print(json.dumps({"op": "waste", "metric": "KV-memory waste fraction (time-averaged)",
+                      "by_block_size": rows,
+                      "config": {"max_len": 2048, "concurrent": 64, "requests": 512,
+                                 "prompt_range": [16, 512], "output": "geometric, mean 200", "seed": 0}}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -384,7 +537,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="decode_step",
+                    choices=["decode_step", "copy_blocks", "block_manager", "serving_step", "waste"],
+                    help="decode_step is the headline; the others print secondary measurements")
     args = ap.parse_args()
+    if args.op != "decode_step":
+        if int(os.environ.get("RANK", "0")) == 0:
+            {"copy_blocks": run_copy_blocks, "block_manager": run_block_manager,
+             "serving_step": run_serving_step, "waste": run_waste}[args.op](args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
