@@ -1,10 +1,11 @@
 #!/usr/bin/env python3
 """Benchmark: one decode step of paged attention per iteration, on GB300.
 
-A step is the whole hot path over one batch: pa_reshape_and_cache writes each
-sequence's newest token into its slot, then pa_decode attends over every
-sequence (the serving order: the new token's K/V is in the cache before the
-attention kernel runs). Default workload: Llama-3-8B-shaped GQA decode
+A step is the whole hot path over one batch: each sequence's newest token is
+written into its slot and attention runs over every sequence (the serving
+order: the new token's K/V is in the cache before attention). By default the
+step is pa_decode_append, which does both in one kernel; ``--step separate``
+runs pa_reshape_and_cache then pa_decode. Default workload: Llama-3-8B-shaped GQA decode
 (128 sequences, 32 query / 8 kv heads, head_dim 128, block size 16, lengths
 uniform in [1024, 8192], bf16, random block placement, seed 0).
 
@@ -258,17 +259,25 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty_like(q)
     ws = pa.alloc_workspace(q, kc, bt, pt)
     stream = torch.cuda.current_stream(dev)
+    fused = args.step == "fused"
 
     def step():
-        pa.reshape_and_cache(nk, nv, kc, vc, slots)
-        pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
+        if fused:  # cache write + attention in one kernel
+            pa.decode_append(out, q, nk, nv, kc, vc, bt, sl, case.scale, pt, ws)
+        else:
+            pa.reshape_and_cache(nk, nv, kc, vc, slots)
+            pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
 
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
 
     dec_bytes = case.algorithmic_bytes()
-    step_bytes = dec_bytes + case.cache_write_bytes()
+    # the step must also store each new K/V row once (its read is already in
+    # dec_bytes as the newest token of its sequence)
+    written = 2 * int((case.slot_mapping >= 0).sum()) * case.num_kv_heads * case.head_dim * 2
+    step_bytes = dec_bytes + written
+    kern_bytes = step_bytes if fused else dec_bytes
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
@@ -284,10 +293,15 @@ def run_ours(args, rank, world, local_rank):
                       int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
         start.record(stream)
         for i in range(K):
-            pa.reshape_and_cache(nk, nv, kc, vc, slots)
-            ev[i][0].record(stream)
-            pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
-            ev[i][1].record(stream)
+            if fused:
+                ev[i][0].record(stream)
+                pa.decode_append(out, q, nk, nv, kc, vc, bt, sl, case.scale, pt, ws)
+                ev[i][1].record(stream)
+            else:
+                pa.reshape_and_cache(nk, nv, kc, vc, slots)
+                ev[i][0].record(stream)
+                pa.decode(out, q, kc, vc, bt, sl, case.scale, pt, ws)
+                ev[i][1].record(stream)
         stop.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -335,28 +349,32 @@ def run_ours(args, rank, world, local_rank):
         return
     peak, peak_kind = _peaks()
     dec_mean_ms = statistics.mean(dec_ms)
-    achieved = dec_bytes / (dec_mean_ms * 1e-3) / 1e9
+    achieved = kern_bytes / (dec_mean_ms * 1e-3) / 1e9
     value = step_bytes * K * world / (ms * 1e-3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
-        "data": "synthetic", "config": _config(case, args) | {"partition_tokens": pt or 512},
+        "data": "synthetic",
+        "config": _config(case, args) | {"partition_tokens": pt or 512,
+                                         "step": "pa_decode_append (one kernel)" if fused else
+                                                 "pa_reshape_and_cache + pa_decode"},
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         **({"unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "unique_kv_GBps": round(case.unique_kv_bytes() * K * world / (ms * 1e-3) / 1e9, 2)}
            if case.name.startswith("shared_prefix") else {}),
         "tokens_per_s": round(case.num_seqs * K * world / (ms * 1e-3), 1),
         "kv_tokens_per_s": round(float(case.seq_lens.sum()) * K * world / (ms * 1e-3), 1),
-        "roofline": {"kernel": "paged_decode_kernel", "bound": "hbm", "achieved": round(achieved, 2),
+        "roofline": {"kernel": "paged_decode_kernel" + (" (cache write fused)" if fused else ""),
+                     "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
-                     "algorithmic_bytes": dec_bytes,
+                     "algorithmic_bytes": kern_bytes,
                      "mean_launch_us": round(dec_mean_ms * 1e3, 2),
                      "median_launch_us": round(statistics.median(dec_ms) * 1e3, 2)},
         "e2e": {"value": round(step_bytes * Ke * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
-        "gpu_launches": 2 * K,
+        "gpu_launches": K if fused else 2 * K,
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
@@ -537,6 +555,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--step", default="fused", choices=["fused", "separate"],
+                    help="fused: pa_decode_append; separate: pa_reshape_and_cache then pa_decode")
     ap.add_argument("--op", default="decode_step",
                     choices=["decode_step", "copy_blocks", "block_manager", "serving_step", "waste"],
                     help="decode_step is the headline; the others print secondary measurements")

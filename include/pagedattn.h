@@ -144,6 +144,28 @@ int pa_decode(void* out, const void* query,
               cudaStream_t stream);
 
 /*
+ * The decode step's cache write and attention in one kernel ("PagedAttention
+ * by hand", Setup, Step 1: the newest token's key and value are in the cache
+ * before attention runs). For every sequence s with L = seq_lens[s] >= 1 and
+ * every kv head h, the row new_key[s, h, :] (new_value likewise) is token
+ * L-1's K (V): the kernel uses it for that token and stores it into its slot
+ * key_cache[block_tables[s, (L-1) / B], (L-1) % B, h, :]. The result and the
+ * caches afterwards are those of pa_reshape_and_cache (slot of token L-1 of
+ * each sequence) followed by pa_decode. new_key, new_value: DEVICE
+ * [S, Hkv, d], 16-byte aligned. The block holding token L-1 must belong to
+ * sequence s alone (resolve copy-on-write first, e.g. with pa_bm_append and
+ * pa_copy_blocks). Other arguments, sizes and errors as for pa_decode.
+ */
+int pa_decode_append(void* out, const void* query, const void* new_key, const void* new_value,
+                     void* key_cache, void* value_cache,
+                     const int32_t* block_tables, const int32_t* seq_lens,
+                     int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                     int block_size, float scale,
+                     int max_blocks_per_seq, int num_blocks, int partition_tokens,
+                     pa_dtype dtype, pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
+/*
  * pa_decode without a caller-provided workspace, for callers that cannot
  * allocate device memory: for example a plugin inside a host runtime that owns
  * every device allocation, or a serving loop that forbids allocation after

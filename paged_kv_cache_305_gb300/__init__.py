@@ -14,6 +14,7 @@ from .pagedattn import (  # noqa: F401
     bad_index_count,
     copy_blocks,
     decode,
+    decode_append,
     decode_no_alloc,
     decode_workspace_bytes,
     last_error,

@@ -212,11 +212,16 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
   return pa::workspace_layout(num_seqs, num_q_heads, head_dim, static_cast<int>(parts)).total;
 }
 
-int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
-              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
-              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
-              int max_blocks_per_seq, int num_blocks, int partition_tokens, pa_dtype dtype,
-              pa_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int decode_impl(void* out, const void* query, const void* key_cache, const void* value_cache,
+                const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+                int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+                int max_blocks_per_seq, int num_blocks, int partition_tokens, pa_dtype dtype,
+                pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                const void* new_key, const void* new_value, cudaStream_t stream) {
   g_error.clear();
   int rc = check_dtype(dtype);
   if (rc != PA_OK) return rc;
@@ -303,6 +308,8 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
   a.max_partitions = parts;
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
+  a.new_key = new_key;
+  a.new_value = new_value;
   char* ws = static_cast<char*>(workspace);
   a.ws_count = wl.total ? reinterpret_cast<int*>(ws + wl.count_off) : nullptr;
   a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
@@ -311,6 +318,39 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
   cudaError_t e = pa::launch_decode(a, head_dim, dtype == PA_BFLOAT16, sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+              const int32_t* block_tables, const int32_t* seq_lens, int num_seqs,
+              int num_q_heads, int num_kv_heads, int head_dim, int block_size, float scale,
+              int max_blocks_per_seq, int num_blocks, int partition_tokens, pa_dtype dtype,
+              pa_dtype out_dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return decode_impl(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, scale, max_blocks_per_seq,
+                     num_blocks, partition_tokens, dtype, out_dtype, workspace, workspace_bytes,
+                     nullptr, nullptr, stream);
+}
+
+int pa_decode_append(void* out, const void* query, const void* new_key, const void* new_value,
+                     void* key_cache, void* value_cache, const int32_t* block_tables,
+                     const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                     int head_dim, int block_size, float scale, int max_blocks_per_seq,
+                     int num_blocks, int partition_tokens, pa_dtype dtype, pa_dtype out_dtype,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  g_error.clear();
+  if (num_seqs > 0) {
+    if (!new_key || !new_value) return fail(PA_ERR_INVALID, "new_key / new_value is NULL");
+    if (!aligned16(new_key) || !aligned16(new_value))
+      return fail(PA_ERR_INVALID, "new_key and new_value must be 16-byte aligned");
+  }
+  return decode_impl(out, query, key_cache, value_cache, block_tables, seq_lens, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, scale, max_blocks_per_seq,
+                     num_blocks, partition_tokens, dtype, out_dtype, workspace, workspace_bytes,
+                     new_key, new_value, stream);
 }
 
 }  // extern "C"

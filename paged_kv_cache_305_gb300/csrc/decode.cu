@@ -65,7 +65,7 @@ struct Seg {
   int ntiles;    // 16-token tiles in the range
   int piece;     // -1: the segment is the whole row; else its piece index
   int npieces;   // pieces of the row (when piece >= 0)
-  int pad;
+  int L;         // the sequence's length
 };
 
 template <int D, int STAGES>
@@ -136,6 +136,7 @@ paged_decode_kernel(const DecodeArgs a) {
   Seg* sSeg = reinterpret_cast<Seg*>(sML + kWarps * 2 * kRows);
   float* sMerge =  // [warp][G][kOS], present only when warps share a head
       reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sSeg) + Geo::kSegBytes);
+  __shared__ int sFresh[kWarps][STAGES];  // per ring slot: block id of the newest token's row, or -1
   __shared__ long long sW[3];  // base position of the first / last unit's row
   __shared__ int sRange[6];    // first unit (hg, s, p), end unit (hg, s, p)
 
@@ -289,7 +290,7 @@ paged_decode_kernel(const DecodeArgs a) {
       g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
       g.piece = -1;
       g.npieces = 1;
-      g.pad = 0;
+      g.L = L;
       if (!(pf == 0 && pl == np)) {
         // a row cut between CTAs: walk its owners in order to find this CTA's
         // piece index and the number of pieces
@@ -346,9 +347,14 @@ paged_decode_kernel(const DecodeArgs a) {
         const int tb = g.t0 + is_j * kTileTokens;
         unsigned char* sk = wpipe + (issued % STAGES) * Geo::kStageBytes;
         unsigned char* sv = sk + Geo::kTileBytes;
-        const size_t hoff = static_cast<size_t>(g.hg * Hc + hi) * D + cc * 8;
+        const int h = g.hg * Hc + hi;
+        const size_t hoff = static_cast<size_t>(h) * D + cc * 8;
         const T* kb = kcache + hoff;
         const T* vb = vcache + hoff;
+        // with new K/V given, the tile holding the sequence's newest token reads
+        // that row from them (and the compute step stores it into its slot)
+        const int fresh_r = (a.new_key != nullptr && g.t1 == g.L) ? g.L - 1 - tb : -1;
+        const size_t nrow = (static_cast<size_t>(g.s) * Hkv + h) * D + cc * 8;
 #pragma unroll
         for (int i = 0; i < kCopies; ++i) {
           const int r = cr + i * kRowsPerCopy;
@@ -359,8 +365,20 @@ paged_decode_kernel(const DecodeArgs a) {
           if (in && !ok && cc == 0) atomicAdd(a.bad, 1ull);  // rejected id: its rows read as zero
           const size_t slot = ok ? (static_cast<size_t>(phys) << shift) + (t & bmask) : 0;
           const uint32_t off = r * kRowBytes + swz(r, cc);
-          cp_async_16(smem_u32(sk + off), kb + slot * slot_stride, ok);
-          cp_async_16(smem_u32(sv + off), vb + slot * slot_stride, ok);
+          if (r == fresh_r) {
+            cp_async_16(smem_u32(sk + off), static_cast<const T*>(a.new_key) + nrow, true);
+            cp_async_16(smem_u32(sv + off), static_cast<const T*>(a.new_value) + nrow, true);
+          } else {
+            cp_async_16(smem_u32(sk + off), kb + slot * slot_stride, ok);
+            cp_async_16(smem_u32(sv + off), vb + slot * slot_stride, ok);
+          }
+        }
+        {
+          const int fp = __shfl_sync(kFull, idq[0], fresh_r >= 0 && fresh_r < kTileTokens ? fresh_r : 0);
+          if (lane == 0)
+            sFresh[warp][issued % STAGES] =
+                (fresh_r >= 0 && fresh_r < kTileTokens &&
+                 static_cast<unsigned>(fp) < static_cast<unsigned>(a.num_blocks)) ? fp : -1;
         }
         ++issued;
         advance(is_sg, is_j);
@@ -387,8 +405,18 @@ paged_decode_kernel(const DecodeArgs a) {
         __syncwarp();
         const unsigned char* sk = wpipe + (consumed % STAGES) * Geo::kStageBytes;
         const unsigned char* sv = sk + Geo::kTileBytes;
+        const int fresh_phys = sFresh[warp][consumed % STAGES];
         ++consumed;
         const int valid = g.t1 - (g.t0 + j * kTileTokens);  // >= 1
+        if (fresh_phys >= 0 && lane < kChunks) {
+          // the step's new K/V row, now in shared memory, goes to its cache slot
+          const int r = g.L - 1 - (g.t0 + j * kTileTokens);
+          const size_t dst = ((static_cast<size_t>(fresh_phys) << shift) + ((g.L - 1) & bmask)) * slot_stride +
+                             static_cast<size_t>(g.hg * Hc + hi) * D + lane * 8;
+          const uint32_t off = r * kRowBytes + swz(r, lane);
+          *reinterpret_cast<uint4*>(const_cast<T*>(kcache) + dst) = *reinterpret_cast<const uint4*>(sk + off);
+          *reinterpret_cast<uint4*>(const_cast<T*>(vcache) + dst) = *reinterpret_cast<const uint4*>(sv + off);
+        }
 
         // scores S^T[token][head] = K q^T: 16 tokens x 8*NT heads. The k-steps
         // alternate between two accumulators to halve the dependent chain.

@@ -30,6 +30,8 @@ struct DecodeArgs {
   int max_partitions;  // ceil(max_blocks_per_seq * block_size / partition_tokens)
   float scale_log2;    // scale * log2(e): scores are kept in base-2 units
   int out_f32;         // 1: out is fp32; 0: out has the input element type
+  const void* new_key;    // [S, Hkv, d] newest token's K/V rows, or null (plain decode)
+  const void* new_value;
   float* ws_out;       // [S, Hq, max_partitions, d] fp32 partial outputs (normalised)
   float* ws_lse;       // [S, Hq, max_partitions] fp32 base-2 log-sum-exp
   int* ws_count;       // [S * Hkv] arrival counters (zero between calls)

@@ -23,7 +23,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_last_error", "pa_bad_index_count", "pa_decode_no_alloc",
             "pa_decode_no_alloc_scratch_bytes", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
-            "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count")
+            "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
+            "pa_decode_append")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -62,6 +63,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_no_alloc.restype = i32
     L.pa_decode_no_alloc_scratch_bytes.argtypes = []
     L.pa_decode_no_alloc_scratch_bytes.restype = sz
+    L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                   ctypes.c_float, i32, i32, i32, i32, i32, vp, sz, vp]
+    L.pa_decode_append.restype = i32
     L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     L.pa_copy_blocks.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -188,6 +192,46 @@ def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
                            ws_ptr, ws_bytes,
                            _stream(query, stream)))
+    return out
+
+
+def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
+                  new_value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: Optional[float] = None,
+                  partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                  stream=None) -> torch.Tensor:
+    """:func:`decode` that also writes each sequence's newest token (position
+    seq_lens-1) from ``new_key`` / ``new_value`` [S, Hkv, d] into its slot, in
+    the same kernel."""
+    S, Hq, d = query.shape
+    NB, B, Hkv, d2 = key_cache.shape
+    _need(new_key.shape == (S, Hkv, d) and new_value.shape == (S, Hkv, d)
+          and new_key.dtype == new_value.dtype == query.dtype, "new_key/new_value shape or dtype mismatch")
+    _need(new_key.is_cuda and new_key.is_contiguous() and new_value.is_contiguous(),
+          "new_key/new_value must be contiguous CUDA tensors")
+    _need(d2 == d and value_cache.shape == key_cache.shape, "cache shape mismatch")
+    _need(out.shape == query.shape and query.dtype == key_cache.dtype == value_cache.dtype
+          and out.dtype in (query.dtype, torch.float32), "out/query/cache dtype or shape mismatch")
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32,
+          "block_tables and seq_lens must be int32")
+    _need(block_tables.dim() == 2 and block_tables.shape[0] == S and seq_lens.shape == (S,),
+          "block_tables/seq_lens shape mismatch")
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    L = load_library()
+    with torch.cuda.device(query.device):
+        _check(L.pa_decode_append(out.data_ptr(), query.data_ptr(), new_key.data_ptr(),
+                                  new_value.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                  block_tables.data_ptr(), seq_lens.data_ptr(), S, Hq, Hkv, d, B,
+                                  float(scale), block_tables.shape[1], NB, partition_tokens,
+                                  _dtype_code(query),
+                                  PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+                                  ws_ptr, ws_bytes, _stream(query, stream)))
     return out
 
 

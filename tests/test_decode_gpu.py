@@ -261,3 +261,37 @@ def test_small_workspace_is_rejected():
     with pytest.raises(pa.PagedAttnError, match="workspace"):
         pa.decode(dc.out, dc.query, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens,
                   case.scale, 0, dc.workspace[:64])
+
+
+APPEND_CASES = [
+    # dtype, d, Hq, Hkv, B, lengths, partition_tokens
+    ("bf16", 128, 32, 8, 16, (1, 3000), 256),
+    ("fp16", 64, 4, 4, 1, (1, 300), 0),
+    ("bf16", 128, 16, 1, 64, (1, 900), 128),
+    ("fp16", 128, 8, 2, 8, (1, 40), 16),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(APPEND_CASES)))
+def test_decode_append_equals_write_then_decode(idx):
+    dtype, d, Hq, Hkv, B, lens, pt = APPEND_CASES[idx]
+    case = W.random_case(num_seqs=9, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
+                         len_range=lens, dtype=dtype, seed=300 + idx, partition_tokens=pt)
+    case.seq_lens[3] = 0  # nothing to write, zero output
+    case.slot_mapping[3] = -1
+    two = DeviceCase(case)
+    two.write_new_tokens()
+    want16 = host_bits(two.decode()).copy()
+    want32 = two.decode(out_f32=True).cpu().numpy().copy()
+    one = DeviceCase(case)
+    for out, want in ((one.out, None), (one.out32, want32)):
+        pa.decode_append(out, one.query, one.new_key, one.new_value, one.key_cache, one.value_cache,
+                         one.block_tables, one.seq_lens, case.scale, pt, one.workspace)
+    assert np.array_equal(host_bits(one.out), want16)
+    assert np.array_equal(one.out32.cpu().numpy(), want32)
+    assert np.array_equal(host_bits(one.key_cache), host_bits(two.key_cache))
+    assert np.array_equal(host_bits(one.value_cache), host_bits(two.value_cache))
+    kc, vc = oracle_after_write(case)
+    ref = oracle.paged_decode(case.query, kc, vc, case.block_tables, case.seq_lens, B,
+                              case.scale, dtype)
+    check_parity(want16, want32, ref, dtype, "decode_append")
