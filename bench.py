@@ -132,6 +132,25 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
+# Multi-process timing: every rank times its own replica; the job's time is the
+# slowest rank's, and value counts the units all ranks processed.
+# ---------------------------------------------------------------------------
+def max_over_ranks(times_ms, dist, device="cpu"):
+    """Element-wise max of this rank's timings over all ranks (identity without dist)."""
+    if dist is None:
+        return [float(t) for t in times_ms]
+    import torch
+    t = torch.tensor([float(x) for x in times_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_throughput(units_per_rank, world, max_ms):
+    """Whole-job throughput: units of all ranks over the slowest rank's time (per second)."""
+    return units_per_rank * world / (max_ms * 1e-3)
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle leg
 # ---------------------------------------------------------------------------
 def _pair_bytes(case, s):
@@ -338,10 +357,7 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     e2e_ms = e0.elapsed_time(e1)
 
-    if dist is not None:
-        t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
 
     if rank != 0:
         if dist is not None:
@@ -350,7 +366,7 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = _peaks()
     dec_mean_ms = statistics.mean(dec_ms)
     achieved = kern_bytes / (dec_mean_ms * 1e-3) / 1e9
-    value = step_bytes * K * world / (ms * 1e-3) / 1e9
+    value = job_throughput(step_bytes * K, world, ms) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms / K, 5),
