@@ -15,6 +15,7 @@ from .paged_attention import (  # noqa: F401
     single_query_attention,
     paged_decode,
     paged_decode_pairs,
+    paged_prefill,
     reshape_and_cache,
     partition_stats,
     combine_partitions,

@@ -183,6 +183,40 @@ def paged_decode_pairs(query, key_cache, value_cache, block_tables, seq_lens,
 
 
 # ---------------------------------------------------------------------------
+# Paged causal prefill (chunked prefill)
+# ---------------------------------------------------------------------------
+def paged_prefill(query, key_cache, value_cache, block_tables, seq_lens, query_start,
+                  block_size: int, scale: float, dtype: str) -> np.ndarray:
+    """Causal attention of a chunk of new tokens over a paged cache, float64.
+
+    ``query`` [total_q, Hq, d]: sequence s owns rows query_start[s] ..
+    query_start[s+1]-1, its Q_s newest tokens; with L = seq_lens[s] (the
+    chunk's K/V already in the cache), query j sits at position L - Q_s + j
+    and attends to tokens 0 .. L - Q_s + j ("PagedAttention" glossary, How It
+    Works: the blockwise formula with query index i, read token by token so
+    every token up to i counts once and none after it). Returns float64
+    [total_q, Hq, d].
+    """
+    total_q, Hq, d = query.shape
+    Hkv = key_cache.shape[2]
+    G = Hq // Hkv
+    out = np.zeros((total_q, Hq, d), dtype=np.float64)
+    for s in range(len(seq_lens)):
+        L = int(seq_lens[s])
+        q0, q1 = int(query_start[s]), int(query_start[s + 1])
+        Q = q1 - q0
+        K = to_float64(gather_kv(key_cache, block_tables[s], L, block_size), dtype)
+        V = to_float64(gather_kv(value_cache, block_tables[s], L, block_size), dtype)
+        for j in range(Q):
+            p = L - Q + j
+            q = to_float64(query[q0 + j], dtype)
+            for h in range(Hkv):
+                o, _ = single_query_attention(q[h * G:(h + 1) * G], K[:p + 1, h, :], V[:p + 1, h, :], scale)
+                out[q0 + j, h * G:(h + 1) * G] = o
+    return out
+
+
+# ---------------------------------------------------------------------------
 # Cache write
 # ---------------------------------------------------------------------------
 def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping,
