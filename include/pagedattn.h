@@ -202,6 +202,28 @@ int pa_decode_no_alloc(void* out, const void* query,
 size_t pa_decode_no_alloc_scratch_bytes(void);
 
 /*
+ * Paged causal prefill (chunked prefill). Sequence s has L = seq_lens[s]
+ * tokens in the cache, the last Q_s of which are new (their K/V already
+ * written, e.g. with pa_reshape_and_cache); their queries are the rows
+ * query_start[s] .. query_start[s+1]-1 of `query`. Query j sits at position
+ * L - Q_s + j and attends to tokens 0 .. L - Q_s + j ("PagedAttention"
+ * glossary, How It Works: the blockwise formula with query index i, read
+ * token by token):
+ *   out[query_start[s] + j, hq, :] = sum_{t <= L-Q_s+j} softmax(scale q.K_t)_t V_t
+ * with K_t / V_t read through the block table as in pa_decode.
+ * query, out: [total_q, Hq, d] (out: dtype or fp32); query_start: DEVICE int32
+ * [num_seqs + 1], non-decreasing, query_start[0] = 0; max_query_len: HOST
+ * upper bound of Q_s (sizes the grid). A Q_s above L or a length above
+ * max_blocks_per_seq * block_size is clamped and counted by
+ * pa_bad_index_count. Other sizes and errors as for pa_decode.
+ */
+int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+               const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
+               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+               float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
+               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream);
+
+/*
  * Block copies inside the pools, the device half of copy-on-write
  * ("PagedAttention by hand", Why divide memory into physical blocks?:
  * allocate a fresh block, copy that one block's contents, write into the

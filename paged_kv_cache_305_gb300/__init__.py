@@ -19,6 +19,7 @@ from .pagedattn import (  # noqa: F401
     decode_workspace_bytes,
     last_error,
     load_library,
+    prefill,
     no_alloc_scratch_bytes,
     reshape_and_cache,
 )

@@ -196,6 +196,70 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* src, const
   return PA_OK;
 }
 
+int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+               const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
+               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+               float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
+               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream) {
+  g_error.clear();
+  int rc = check_dtype(dtype);
+  if (rc != PA_OK) return rc;
+  if (out_dtype != dtype && out_dtype != PA_FLOAT32)
+    return fail(PA_ERR_INVALID, "out_dtype %d must equal dtype %d or be PA_FLOAT32", (int)out_dtype,
+                (int)dtype);
+  if (num_seqs < 0) return fail(PA_ERR_INVALID, "num_seqs %d < 0", num_seqs);
+  if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
+    return fail(PA_ERR_INVALID, "num_q_heads %d must be a positive multiple of num_kv_heads %d",
+                num_q_heads, num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  if (group > pa::kMaxGroup)
+    return fail(PA_ERR_UNSUPPORTED, "%d query heads per kv head (> %d)", group, pa::kMaxGroup);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  const int shift = log2_pow2(block_size);
+  if (shift < 0)
+    return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two up to 64)", block_size);
+  if (max_blocks_per_seq < 1 || num_blocks < 1)
+    return fail(PA_ERR_INVALID, "max_blocks_per_seq and num_blocks must be >= 1");
+  if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffll)
+    return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size overflows int");
+  if (!isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
+  if (max_query_len < 0) return fail(PA_ERR_INVALID, "max_query_len %d < 0", max_query_len);
+  if (num_seqs > 65535 || num_kv_heads > 65535)
+    return fail(PA_ERR_UNSUPPORTED, "num_seqs %d / num_kv_heads %d above 65535", num_seqs, num_kv_heads);
+  if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+  if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !query_start)
+    return fail(PA_ERR_INVALID, "a pointer argument is NULL");
+  if (!aligned16(out) || !aligned16(query) || !aligned16(key_cache) || !aligned16(value_cache))
+    return fail(PA_ERR_INVALID, "out, query and the caches must be 16-byte aligned");
+  if (!aligned4(block_tables) || !aligned4(seq_lens) || !aligned4(query_start))
+    return fail(PA_ERR_INVALID, "block_tables, seq_lens and query_start must be 4-byte aligned");
+  unsigned long long* bad = nullptr;
+  rc = bad_counter(&bad);
+  if (rc != PA_OK) return rc;
+  pa::PrefillArgs a{};
+  a.out = out;
+  a.query = query;
+  a.key_cache = key_cache;
+  a.value_cache = value_cache;
+  a.block_tables = block_tables;
+  a.seq_lens = seq_lens;
+  a.query_start = query_start;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.group = group;
+  a.block_shift = shift;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.num_blocks = num_blocks;
+  a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
+  a.bad = bad;
+  cudaError_t e = pa::launch_prefill(a, head_dim, dtype == PA_BFLOAT16, max_query_len, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  return PA_OK;
+}
+
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size, int partition_tokens) {
   if (num_seqs < 0 || num_q_heads < 1 || (head_dim != 64 && head_dim != 128) ||

@@ -38,6 +38,29 @@ struct DecodeArgs {
   unsigned long long* bad;  // device counter of rejected indices
 };
 
+struct PrefillArgs {
+  void* out;                  // [total_q, Hq, d]
+  const void* query;          // [total_q, Hq, d]
+  const void* key_cache;
+  const void* value_cache;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* query_start;  // [S + 1]
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int group;
+  int block_shift;
+  int max_blocks_per_seq;
+  int num_blocks;
+  float scale_log2;
+  int out_f32;
+  unsigned long long* bad;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
+                           cudaStream_t stream);
+
 // Records `msg` as the calling thread's last error and returns `code`;
 // clear_error() empties it (entry points call it first).
 int set_error(int code, const char* msg);

@@ -24,7 +24,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_decode_no_alloc_scratch_bytes", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
             "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
-            "pa_decode_append")
+            "pa_decode_append", "pa_prefill")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -66,6 +66,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_decode_append.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                    ctypes.c_float, i32, i32, i32, i32, i32, vp, sz, vp]
     L.pa_decode_append.restype = i32
+    L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
+                             i32, i32, i32, i32, i32, vp]
+    L.pa_prefill.restype = i32
     L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     L.pa_copy_blocks.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -232,6 +235,41 @@ def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
                                   _dtype_code(query),
                                   PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
                                   ws_ptr, ws_bytes, _stream(query, stream)))
+    return out
+
+
+def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+            value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+            query_start: torch.Tensor, max_query_len: int, scale: Optional[float] = None,
+            stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's newest tokens over the paged cache.
+
+    ``query``/``out`` [total_q, Hq, d]; sequence s owns query rows
+    query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its newest tokens,
+    whose K/V are already in the cache; ``max_query_len`` bounds the rows per
+    sequence.
+    """
+    total_q, Hq, d = query.shape
+    NB, B, Hkv, d2 = key_cache.shape
+    S = seq_lens.shape[0]
+    _need(d2 == d and value_cache.shape == key_cache.shape, "cache shape mismatch")
+    _need(out.shape == query.shape and query.dtype == key_cache.dtype == value_cache.dtype
+          and out.dtype in (query.dtype, torch.float32), "out/query/cache dtype or shape mismatch")
+    _need(block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
+          and query_start.dtype == torch.int32, "block_tables, seq_lens, query_start must be int32")
+    _need(block_tables.shape[0] == S and query_start.shape == (S + 1,), "shape mismatch")
+    for t in (out, query, key_cache, value_cache, block_tables, seq_lens, query_start):
+        _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    L = load_library()
+    with torch.cuda.device(query.device):
+        _check(L.pa_prefill(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
+                            value_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(),
+                            query_start.data_ptr(), S, Hq, Hkv, d, B, float(scale),
+                            block_tables.shape[1], NB, int(max_query_len), _dtype_code(query),
+                            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+                            _stream(query, stream)))
     return out
 
 

@@ -1,0 +1,80 @@
+"""GPU parity of pa_prefill (paged causal prefill, through the C ABI) against
+the float64 oracle: chunks of new tokens of several lengths (one token, part
+of a prompt, a whole prompt), several query tiles and key tiles per sequence,
+ragged tails, every group size path and block size."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import oracle
+import paged_kv_cache_305_gb300 as pa
+import workloads as W
+from gpu_util import ATOL, DeviceCase, check_parity, dev_bits, host_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_305_gb300 import build
+    build.build()
+    yield
+    torch.cuda.synchronize()
+
+
+def _run(case, qlens, seed):
+    starts = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    q = W.normal_bits((int(starts[-1]), case.num_q_heads, case.head_dim), case.dtype, seed, 55)
+    dc = DeviceCase(case)
+    qd = dev_bits(q, case.dtype)
+    qs = torch.from_numpy(starts).cuda()
+    out16 = torch.empty_like(qd)
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    mq = int(max(qlens))
+    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, case.scale)
+    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, case.scale)
+    ref = oracle.paged_prefill(q, case.key_cache, case.value_cache, case.block_tables, case.seq_lens,
+                               starts, case.block_size, case.scale, case.dtype)
+    check_parity(host_bits(out16), out32.cpu().numpy(), ref, case.dtype, f"prefill {case.name}")
+    return q, out32.cpu().numpy()
+
+
+CASES = [
+    # dtype, d, Hq, Hkv, B, lengths
+    ("bf16", 128, 32, 8, 16, (40, 700)),
+    ("fp16", 64, 4, 4, 1, (1, 200)),
+    ("bf16", 128, 16, 1, 64, (100, 500)),
+    ("fp16", 128, 12, 4, 8, (1, 150)),
+    ("bf16", 64, 16, 2, 16, (70, 300)),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(CASES)))
+def test_prefill_chunks(idx):
+    dtype, d, Hq, Hkv, B, lens = CASES[idx]
+    case = W.random_case(num_seqs=5, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
+                         len_range=lens, dtype=dtype, seed=400 + idx)
+    L = case.seq_lens
+    # a whole prompt, one token, a partial chunk, a zero-length chunk, a ragged chunk
+    qlens = [int(L[0]), 1, max(1, int(L[2]) // 3), 0, min(int(L[4]), 77)]
+    _run(case, qlens, idx)
+
+
+def test_single_token_chunks_match_decode():
+    case = W.random_case(num_seqs=6, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                         len_range=(1, 900), dtype="bf16", seed=7)
+    q, got = _run(case, [1] * 6, 3)
+    dc = DeviceCase(case)
+    out32 = torch.empty((6, 32, 128), dtype=torch.float32, device="cuda")
+    pa.decode(out32, dev_bits(q, "bf16"), dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens,
+              case.scale, 0, dc.workspace)
+    assert np.max(np.abs(out32.cpu().numpy() - got)) <= ATOL
+
+
+def test_long_prompt_many_tiles():
+    case = W.random_case(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                         len_range=(1500, 1500), dtype="bf16", seed=8)
+    _run(case, [1500, 1000], 5)
