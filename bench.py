@@ -555,6 +555,41 @@ def run_waste(args):
                                  "prompt_range": [16, 512], "output": "geometric, mean 200", "seed": 0}}))
 
 
+def run_prefill(args):
+    """Paged causal prefill: algorithmic TFLOP/s (4 * d * Hq per causal pair)."""
+    import torch
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    S, Hq, Hkv, d, B = 16, 32, 8, 128, 16
+    ctx, chunk = args.prefill_context, args.prefill_chunk
+    case = W.random_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
+                         len_range=(ctx, ctx), dtype="bf16", seed=0)
+    dt = torch.bfloat16
+    up = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(dt)
+    kc, vc = up(case.key_cache), up(case.value_cache)
+    bt = torch.from_numpy(case.block_tables).cuda()
+    sl = torch.from_numpy(case.seq_lens).cuda()
+    starts = torch.arange(0, (S + 1) * chunk, chunk, dtype=torch.int32).cuda()
+    q = torch.randn((S * chunk, Hq, d), device="cuda").to(dt)
+    out = torch.empty_like(q)
+    ms = _events(lambda: pa.prefill(out, q, kc, vc, bt, sl, starts, chunk, case.scale),
+                 args.steps, max(3, args.warmup))
+    pairs = S * sum(ctx - chunk + j + 1 for j in range(chunk))
+    flops = 4.0 * d * Hq * pairs
+    tf = flops / (ms * 1e-3) / 1e12
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = float(json.load(open(p))["bf16_tflops"]) if os.path.exists(p) else 1900.0
+    print(json.dumps({"op": "prefill", "metric": "paged causal prefill TFLOP/s (algorithmic)",
+                      "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
+                                   "peak_kind": "measured bf16_tflops (cuBLAS, burst)",
+                                   "frac": round(tf / peak, 4)},
+                      "tokens_per_s": round(S * chunk / (ms * 1e-3), 1), "steps": args.steps,
+                      "config": {"sequences": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
+                                 "block_size": B, "context": ctx, "chunk": chunk, "dtype": "bf16"}}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,16 +606,20 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-context", type=int, default=4096)
+    ap.add_argument("--prefill-chunk", type=int, default=2048)
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
                     help="fused: pa_decode_append; separate: pa_reshape_and_cache then pa_decode")
     ap.add_argument("--op", default="decode_step",
-                    choices=["decode_step", "copy_blocks", "block_manager", "serving_step", "waste"],
+                    choices=["decode_step", "copy_blocks", "block_manager", "serving_step", "waste",
+                             "prefill"],
                     help="decode_step is the headline; the others print secondary measurements")
     args = ap.parse_args()
     if args.op != "decode_step":
         if int(os.environ.get("RANK", "0")) == 0:
             {"copy_blocks": run_copy_blocks, "block_manager": run_block_manager,
-             "serving_step": run_serving_step, "waste": run_waste}[args.op](args)
+             "serving_step": run_serving_step, "waste": run_waste,
+             "prefill": run_prefill}[args.op](args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
