@@ -216,6 +216,8 @@ size_t pa_decode_no_alloc_scratch_bytes(void);
  * upper bound of Q_s (sizes the grid). A Q_s above L or a length above
  * max_blocks_per_seq * block_size is clamped and counted by
  * pa_bad_index_count. Other sizes and errors as for pa_decode.
+ * Block sizes 8..64 (with fewer than 2^31 slots) run on the tcgen05 tensor
+ * cores with TMA block copies; block sizes 1..4 on the warp-level products.
  */
 int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
@@ -305,6 +307,18 @@ const char* pa_last_error(void);
  * Errors: PA_ERR_INVALID (count is NULL), PA_ERR_CUDA.
  */
 int pa_bad_index_count(unsigned long long* count, int clear);
+
+/*
+ * Number of bounded waits inside the kernels on the CURRENT device that gave
+ * up since the counter was last cleared. The tensor-core prefill kernel's
+ * warps wait on each other through shared-memory barriers; every such wait
+ * has a limit of about one second, after which the kernel counts it here and
+ * winds down instead of hanging (its output is then invalid). Always 0 in
+ * correct operation. Synchronises the device; *count is a host pointer;
+ * clears the counter when `clear` is non-zero.
+ * Errors: PA_ERR_INVALID (count is NULL), PA_ERR_CUDA.
+ */
+int pa_wait_timeout_count(unsigned long long* count, int clear);
 
 #ifdef __cplusplus
 }

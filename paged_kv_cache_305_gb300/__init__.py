@@ -22,4 +22,5 @@ from .pagedattn import (  # noqa: F401
     prefill,
     no_alloc_scratch_bytes,
     reshape_and_cache,
+    wait_timeout_count,
 )

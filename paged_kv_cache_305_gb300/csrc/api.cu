@@ -39,11 +39,14 @@ int log2_pow2(int b) {  // -1 unless b is a power of two in [1, 64]
   return -1;
 }
 
-// Device-resident counter of out-of-range indices the kernels skipped.
+// Device-resident counters: out-of-range indices the kernels skipped, and
+// bounded waits (tensor-core prefill) that gave up.
 __device__ unsigned long long g_bad_index_count;
+__device__ unsigned long long g_wait_timeout_count;
 
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned long long*> g_bad_ptr[kMaxDevices];
+std::atomic<unsigned long long*> g_timeout_ptr[kMaxDevices];
 std::atomic<int> g_num_sms[kMaxDevices];
 
 int num_sms(int* out) {
@@ -61,18 +64,39 @@ int num_sms(int* out) {
   return PA_OK;
 }
 
-int bad_counter(unsigned long long** out) {
+// Device address of one of the two counters on the current device (cached).
+int counter(bool timeouts, unsigned long long** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index %d", dev);
-  unsigned long long* p = g_bad_ptr[dev].load(std::memory_order_acquire);
+  std::atomic<unsigned long long*>& slot = timeouts ? g_timeout_ptr[dev] : g_bad_ptr[dev];
+  unsigned long long* p = slot.load(std::memory_order_acquire);
   if (p == nullptr) {
-    e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_bad_index_count);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(bad-index counter)");
-    g_bad_ptr[dev].store(p, std::memory_order_release);
+    e = timeouts ? cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_wait_timeout_count)
+                 : cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_bad_index_count);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(counter)");
+    slot.store(p, std::memory_order_release);
   }
   *out = p;
+  return PA_OK;
+}
+
+int bad_counter(unsigned long long** out) { return counter(false, out); }
+
+int read_counter(bool timeouts, unsigned long long* count, int clear) {
+  if (count == nullptr) return fail(PA_ERR_INVALID, "count is NULL");
+  unsigned long long* p = nullptr;
+  int rc = counter(timeouts, &p);
+  if (rc != PA_OK) return rc;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(count, p, sizeof(*count), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(counter)");
+  if (clear) {
+    e = cudaMemset(p, 0, sizeof(*p));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counter)");
+  }
   return PA_OK;
 }
 
@@ -120,19 +144,12 @@ const char* pa_last_error(void) { return g_error.c_str(); }
 
 int pa_bad_index_count(unsigned long long* count, int clear) {
   g_error.clear();
-  if (count == nullptr) return fail(PA_ERR_INVALID, "count is NULL");
-  unsigned long long* p = nullptr;
-  int rc = bad_counter(&p);
-  if (rc != PA_OK) return rc;
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
-  e = cudaMemcpy(count, p, sizeof(*count), cudaMemcpyDeviceToHost);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(bad-index counter)");
-  if (clear) {
-    e = cudaMemset(p, 0, sizeof(*p));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(bad-index counter)");
-  }
-  return PA_OK;
+  return read_counter(false, count, clear);
+}
+
+int pa_wait_timeout_count(unsigned long long* count, int clear) {
+  g_error.clear();
+  return read_counter(true, count, clear);
 }
 
 int pa_reshape_and_cache(const void* key, const void* value, void* key_cache, void* value_cache,
@@ -255,8 +272,17 @@ int pa_prefill(void* out, const void* query, const void* key_cache, const void* 
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
   a.bad = bad;
-  cudaError_t e = pa::launch_prefill(a, head_dim, dtype == PA_BFLOAT16, max_query_len, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  rc = counter(true, &a.timeouts);
+  if (rc != PA_OK) return rc;
+  const bool bf16 = dtype == PA_BFLOAT16;
+  cudaError_t e;
+  if (pa::prefill_tc_supported(block_size, static_cast<long long>(num_blocks) * block_size)) {
+    e = pa::launch_prefill_tc(a, head_dim, bf16, max_query_len, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "paged prefill (tensor-core) launch");
+  } else {
+    e = pa::launch_prefill(a, head_dim, bf16, max_query_len, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
+  }
   return PA_OK;
 }
 

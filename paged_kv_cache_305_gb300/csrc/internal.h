@@ -56,10 +56,15 @@ struct PrefillArgs {
   float scale_log2;
   int out_f32;
   unsigned long long* bad;
+  unsigned long long* timeouts;  // bounded waits that gave up (tensor-core kernel)
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
                            cudaStream_t stream);
+// Tensor-core (tcgen05 + TMA) prefill: block sizes 8..64, fewer than 2^31 slots.
+bool prefill_tc_supported(int block_size, long long num_slots);
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
+                              cudaStream_t stream);
 
 // Records `msg` as the calling thread's last error and returns `code`;
 // clear_error() empties it (entry points call it first).

@@ -1,0 +1,502 @@
+// Paged causal prefill on the tcgen05 tensor cores (block sizes 8..64).
+//
+// Same operation as the other prefill kernel ("PagedAttention" glossary, How
+// It Works: the blockwise formula with query index i, read token by token):
+// query j of sequence s's Q-token chunk sits at position L - Q + j and
+// attends to tokens 0 .. L - Q + j of the paged cache.
+//
+// One CTA per (query tile, kv head, sequence). A query tile is 128 rows =
+// 128 / G positions x the G heads of the kv head (the product's M), so each
+// K/V tile serves every query head of the group. Key tiles are 64 tokens.
+// Roles (6 warps):
+//   warps 0-3  one thread per query row: loads the query tile, then for every
+//              key tile reads its row of S = q K^T from tensor memory, applies
+//              the causal limit, keeps the running max / sum (base 2), writes
+//              the weights back into tensor memory as a 16-bit head plus the
+//              16-bit rounding of the remainder, and rescales its output row
+//              when the max has grown by more than 2^8 since the last rescale;
+//              finally divides by the sum and stores the row.
+//   warp 4     producer: whole blocks of the tile by TMA (one box per block
+//              and 64-element half of the head dim, straight from the block
+//              table), partial / out-of-range blocks by plain loads with zero
+//              fill; two stages.
+//   warp 5     one thread issues the products: S_j = Q K_j^T (smem x smem,
+//              M=128, N=64) into one of two S column ranges, and
+//              O += P_j V_j (weights from tensor memory, V from smem read
+//              MN-major, N = head dim) for the head and the remainder.
+// Tensor memory (256 columns): S0 at 0, S1 at 64 (each later overwritten by
+// its weights), O at 128. All waits are bounded; a wait that gives up is
+// counted and the CTA winds down without hanging.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kRows = 128;  // query rows per CTA = product M
+constexpr int kKeys = 64;   // tokens per key tile = N of S
+constexpr int kStages = 2;
+constexpr int kThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColO = 128;
+constexpr float kRescaleLog2 = 8.f;
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int D>
+struct TcGeo {
+  static constexpr int kHalves = D / 64;           // 128-byte row slices of the head dim
+  static constexpr int kQHalf = kRows * 128;        // one slice of the query tile
+  static constexpr int kQBytes = kHalves * kQHalf;
+  static constexpr int kTileHalf = kKeys * 128;     // one slice of a K or V tile
+  static constexpr int kTileBytes = kHalves * kTileHalf;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
+  // barriers + alignment slack; at least 80 KB so that no more than two CTAs
+  // (2 x 256 tensor-memory columns) share an SM
+  static constexpr int kSmem = kBarOff + 128 + 1024 > 80 * 1024 ? kBarOff + 128 + 1024 : 80 * 1024;
+};
+static_assert(kStages == 2, "stage and S buffer of tile j are both j & 1");
+
+// barrier slots (8 bytes each) after the tiles
+enum : int {
+  kBarKFull = 0,   // [2]
+  kBarVFull = 2,   // [2]
+  kBarEmpty = 4,   // [2]
+  kBarSFull = 6,   // [2]
+  kBarPFull = 8,   // [2]
+  kBarODone = 10,
+  kBarQFull = 11,
+  kBarDone = 12,
+  kTmemSlot = 13,  // 4-byte TMEM base address
+};
+
+// Offset of 16-byte chunk (chunk & 7) of row `row` inside one 128-byte-row
+// slice (the slice itself, chunk >> 3, is added by the caller).
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Bounded wait made uniform across the warp: every lane of a warp that
+// executes warp-collective tensor-memory instructions must take the same path.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  return __all_sync(kFull, tc::mbar_wait(bar, parity));
+}
+
+template <typename Ty, int D>
+__global__ void __launch_bounds__(kThreads, 2)
+paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  using Geo = TcGeo<D>;
+  using T = typename Ty::T;
+  constexpr int kChunks = D / 8;  // 16-byte chunks per row
+  constexpr int kKSteps = D / 16;
+
+  const int qt = gridDim.x - 1 - blockIdx.x;  // longest tiles first
+  const int h = blockIdx.y;
+  const int s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = a.group;
+  const int P = kRows / G;  // query positions per tile
+  const int shift = a.block_shift;
+  const int Lmax = a.max_blocks_per_seq << shift;
+
+  int L = a.seq_lens[s];
+  const int q0 = a.query_start[s];
+  int Q = a.query_start[s + 1] - q0;
+  if (L < 0 || L > Lmax || Q < 0 || Q > L) {
+    if (qt == 0 && h == 0 && tid == 0) atomicAdd(a.bad, 1ull);
+    L = min(max(L, 0), Lmax);
+    Q = min(max(Q, 0), L);
+  }
+  const int j0 = qt * P;
+  if (j0 >= Q) return;
+  const int jn = min(P, Q - j0);
+  const int last_pos = L - Q + j0 + jn - 1;
+  const int ntiles = last_pos / kKeys + 1;
+
+  extern __shared__ unsigned char raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sQ = tc::smem_u32(sm);
+  const uint32_t sKV = sQ + Geo::kQBytes;
+  const uint32_t bars = sQ + Geo::kBarOff;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  auto sK = [&](int st) { return sKV + static_cast<uint32_t>(st * Geo::kStageBytes); };
+  auto sV = [&](int st) { return sK(st) + static_cast<uint32_t>(Geo::kTileBytes); };
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(bar(kBarKFull + i), 1);
+      tc::mbar_init(bar(kBarVFull + i), 1);
+      tc::mbar_init(bar(kBarEmpty + i), 1);
+      tc::mbar_init(bar(kBarSFull + i), 1);
+      tc::mbar_init(bar(kBarPFull + i), 128);
+    }
+    tc::mbar_init(bar(kBarODone), 1);
+    tc::mbar_init(bar(kBarQFull), 128);
+    tc::mbar_init(bar(kBarDone), 1);
+    tc::mbar_init_fence();
+  }
+  if (warp == 0) tc::tmem_alloc(bar(kTmemSlot), kTmemCols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kBarOff + 8 * kTmemSlot);
+  bool ok = true;
+
+  if (warp < 4) {
+    // ---------------- query tile: row r = (position j0 + r / G, head h*G + r % G)
+    const T* qb = static_cast<const T*>(a.query);
+    for (int i = tid; i < kRows * kChunks; i += 128) {
+      const int r = i / kChunks, c = i % kChunks;
+      const int jj = r / G, g = r % G;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (r < P * G && jj < jn) {
+        const size_t row = static_cast<size_t>(q0 + j0 + jj) * a.num_q_heads +
+                           static_cast<size_t>(h) * G + g;
+        v = __ldg(reinterpret_cast<const uint4*>(qb + row * D) + c);
+      }
+      st_shared_v4(sQ + (c >> 3) * Geo::kQHalf + sw_off(r, c), v);
+    }
+    tc::fence_async_smem();
+    tc::mbar_arrive(bar(kBarQFull));
+
+    // ---------------- softmax: thread tid owns query row tid (TMEM lane tid)
+    const int r = tid;
+    const bool row_valid = r < P * G && r / G < jn;
+    const int qp = row_valid ? L - Q + j0 + r / G : last_pos;  // causal limit
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sl2 = a.scale_log2;
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      const uint32_t colS = static_cast<uint32_t>(b * kKeys);
+      ok = warp_wait(bar(kBarSFull + b), (j >> 1) & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      float sv[kKeys];
+      {
+        uint32_t x0[16], x1[16], x2[16], x3[16];
+        tc::tmem_ld16(lane_addr + colS, x0);
+        tc::tmem_ld16(lane_addr + colS + 16, x1);
+        tc::tmem_ld16(lane_addr + colS + 32, x2);
+        tc::tmem_ld16(lane_addr + colS + 48, x3);
+        tc::tmem_ld_wait16(x0);
+        tc::tmem_ld_wait16(x1);
+        tc::tmem_ld_wait16(x2);
+        tc::tmem_ld_wait16(x3);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sv[i] = __uint_as_float(x0[i]);
+          sv[16 + i] = __uint_as_float(x1[i]);
+          sv[32 + i] = __uint_as_float(x2[i]);
+          sv[48 + i] = __uint_as_float(x3[i]);
+        }
+      }
+      const int kb = j * kKeys;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kKeys; ++c) {
+        const float x = kb + c <= qp ? sv[c] * sl2 : -INFINITY;
+        sv[c] = x;
+        mx = fmaxf(mx, x);
+      }
+      const float mn = fmaxf(m, mx);
+      if (__any_sync(kFull, mn > m + kRescaleLog2)) {
+        const float alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
+        if (j > 0) {
+          // the previous tile's P V must have landed before O is rescaled
+          ok = warp_wait(bar(kBarODone), (j - 1) & 1);
+          if (!ok) break;
+          tc::tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t x[16];
+            tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
+            tc::tmem_ld_wait16(x);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
+            tc::tmem_st16(lane_addr + kColO + 16 * c, x);
+          }
+        }
+        l *= alpha;
+        m = mn;
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t ph[16], pl[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(sv[hh * 32 + 2 * i] - m);
+          const float p1 = ex2(sv[hh * 32 + 2 * i + 1] - m);
+          rs += p0 + p1;
+          ph[i] = Ty::pack(p0, p1);
+          const float2 d = Ty::unpack(ph[i]);
+          pl[i] = Ty::pack(p0 - d.x, p1 - d.y);
+        }
+        tc::tmem_st16(lane_addr + colS + 16 * hh, ph);       // weights, head part
+        tc::tmem_st16(lane_addr + colS + 32 + 16 * hh, pl);  // weights, remainder
+      }
+      l += rs;
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kBarPFull + b));
+    }
+    if (ok) ok = warp_wait(bar(kBarODone), (ntiles - 1) & 1);
+    if (ok) {
+      tc::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row = static_cast<size_t>(q0 + j0 + r / G) * a.num_q_heads +
+                         static_cast<size_t>(h) * G + r % G;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t x[16];
+        tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
+        tc::tmem_ld_wait16(x);
+        if (!row_valid) continue;
+        if (a.out_f32) {
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D + 16 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[i] = make_float4(__uint_as_float(x[4 * i]) * inv, __uint_as_float(x[4 * i + 1]) * inv,
+                               __uint_as_float(x[4 * i + 2]) * inv,
+                               __uint_as_float(x[4 * i + 3]) * inv);
+        } else {
+          uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D + 16 * c);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint4 w;
+            w.x = Ty::pack(__uint_as_float(x[8 * i]) * inv, __uint_as_float(x[8 * i + 1]) * inv);
+            w.y = Ty::pack(__uint_as_float(x[8 * i + 2]) * inv, __uint_as_float(x[8 * i + 3]) * inv);
+            w.z = Ty::pack(__uint_as_float(x[8 * i + 4]) * inv, __uint_as_float(x[8 * i + 5]) * inv);
+            w.w = Ty::pack(__uint_as_float(x[8 * i + 6]) * inv, __uint_as_float(x[8 * i + 7]) * inv);
+            o[i] = w;
+          }
+        }
+      }
+    }
+  } else if (warp == kProducerWarp) {
+    // ---------------- producer: K and V tiles of 64 tokens through the block table
+    const int B = 1 << shift;
+    const int nb = kKeys >> shift;  // blocks per tile (1..8)
+    const int32_t* trow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
+    const T* kc = static_cast<const T*>(a.key_cache);
+    const T* vc = static_cast<const T*>(a.value_cache);
+    const size_t slot_stride = static_cast<size_t>(a.num_kv_heads) * D;
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int st = j & 1;
+      if (j >= kStages) {
+        ok = warp_wait(bar(kBarEmpty + st), ((j >> 1) - 1) & 1);
+        if (!ok) break;
+      }
+      int id = -1, valid = 0;
+      if (lane < nb) {
+        const int blk = j * nb + lane;
+        valid = min(max(L - (blk << shift), 0), B);
+        if (valid > 0) {
+          id = __ldg(trow + blk);
+          if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+            atomicAdd(a.bad, 1ull);
+            id = -1;
+          }
+        }
+      }
+      const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
+      // blocks that are not whole and valid: copy their rows (zeros past L)
+      for (int i = 0; i < nb; ++i) {
+        const int idi = __shfl_sync(kFull, id, i);
+        const int vi = __shfl_sync(kFull, valid, i);
+        if ((whole >> i) & 1u) continue;
+        for (int idx = lane; idx < B * kChunks; idx += 32) {
+          const int t = idx / kChunks, c = idx % kChunks;
+          const int row = i * B + t;
+          uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+          if (idi >= 0 && t < vi) {
+            const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
+                               static_cast<size_t>(h) * D + c * 8;
+            kv = __ldg(reinterpret_cast<const uint4*>(kc + off));
+            vv = __ldg(reinterpret_cast<const uint4*>(vc + off));
+          }
+          const uint32_t so = (c >> 3) * Geo::kTileHalf + sw_off(row, c);
+          st_shared_v4(sK(st) + so, kv);
+          st_shared_v4(sV(st) + so, vv);
+        }
+      }
+      tc::fence_async_smem();
+      __syncwarp();
+      const uint32_t bytes = static_cast<uint32_t>(__popc(whole)) * B * D * 2;
+      if (lane == 0) {
+        tc::mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
+        tc::mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+      }
+      for (int i = 0; i < nb; ++i) {
+        const int idi = __shfl_sync(kFull, id, i);
+        if (lane != 0 || !((whole >> i) & 1u)) continue;
+#pragma unroll
+        for (int hf = 0; hf < Geo::kHalves; ++hf) {
+          const uint32_t dst = static_cast<uint32_t>(hf * Geo::kTileHalf + i * B * 128);
+          tc::tma_load_3d(sK(st) + dst, &kmap, bar(kBarKFull + st), hf * 64, h, idi * B);
+          tc::tma_load_3d(sV(st) + dst, &vmap, bar(kBarVFull + st), hf * 64, h, idi * B);
+        }
+      }
+    }
+    // copies still in flight (only after a wait gave up) must land before exit
+    for (int jj = max(0, j - kStages); jj < j; ++jj) {
+      tc::mbar_wait(bar(kBarKFull + (jj & 1)), (jj >> 1) & 1);
+      tc::mbar_wait(bar(kBarVFull + (jj & 1)), (jj >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
+    // ---------------- products, one thread
+    const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
+    const uint32_t id_o = tc::idesc_f16(kRows, D, Ty::kIsBf16, true);
+    auto issue_s = [&](int j) {
+      const int st = j & 1;
+      const uint32_t d = tmem + static_cast<uint32_t>(st * kKeys);
+#pragma unroll
+      for (int ks = 0; ks < kKSteps; ++ks) {
+        const uint32_t koff = static_cast<uint32_t>((ks & 3) * 32);  // 16 elements = 32 bytes
+        const uint64_t da = tc::sdesc_sw128(sQ + (ks >> 2) * Geo::kQHalf + koff, 16, 1024);
+        const uint64_t db = tc::sdesc_sw128(sK(st) + (ks >> 2) * Geo::kTileHalf + koff, 16, 1024);
+        tc::mma_ss(d, da, db, id_s, ks > 0 ? 1u : 0u);
+      }
+      tc::tc_commit(bar(kBarSFull + st));
+    };
+    ok = tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
+    if (ok) {
+      tc::tc_fence_after();
+      issue_s(0);
+    }
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int b = j & 1;
+      if (j + 1 < ntiles) {
+        // S_{j+1} overwrites the columns that held P_{j-1}: wait for P_{j-1} V
+        if (j >= 1) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1);
+        if (ok) ok = tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+        if (!ok) break;
+        tc::tc_fence_after();
+        issue_s(j + 1);
+      }
+      ok = tc::mbar_wait(bar(kBarPFull + b), (j >> 1) & 1) &&
+           tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      const uint32_t colS = tmem + static_cast<uint32_t>(b * kKeys);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // weights: head part, then remainder
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks) {
+          // V read MN-major: 8-token groups 1024 bytes apart (SBO), the two
+          // 64-element slices of the head dim kTileHalf apart (LBO)
+          const uint64_t dv =
+              tc::sdesc_sw128(sV(b) + ks * 2048, Geo::kHalves > 1 ? Geo::kTileHalf : 16, 1024);
+          tc::mma_ts(tmem + kColO, colS + part * 32 + ks * 8, dv, id_o,
+                     (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      tc::tc_commit(bar(kBarODone));
+      tc::tc_commit(bar(kBarEmpty + b));
+    }
+    // nothing this thread issued may still be running when the CTA ends
+    tc::tc_commit(bar(kBarDone));
+    tc::mbar_wait(bar(kBarDone), 0);
+  }
+
+  if (!ok && lane == 0) atomicAdd(a.timeouts, 1ull);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (f == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && p != nullptr) {
+      f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      fn.store(f, std::memory_order_release);
+    }
+  }
+  return f;
+}
+
+// One cache viewed as [num_blocks * B slots, Hkv, d]; a box is one block of
+// one kv head, 64 elements of the head dim wide, 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, int num_slots, int hkv, int d,
+                      int block_size) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
+                              static_cast<cuuint64_t>(num_slots)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(hkv) * d * 2};
+  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size)};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+             const_cast<void*>(cache), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename Ty, int D>
+cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stream) {
+  const int P = kRows / a.group;
+  const int tiles = (max_query_len + P - 1) / P;
+  if (tiles < 1) return cudaSuccess;
+  const long long slots = static_cast<long long>(a.num_blocks) << a.block_shift;
+  CUtensorMap km, vm;
+  if (!encode_cache_map(&km, a.key_cache, Ty::kIsBf16, static_cast<int>(slots), a.num_kv_heads, D,
+                        1 << a.block_shift) ||
+      !encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, static_cast<int>(slots), a.num_kv_heads,
+                        D, 1 << a.block_shift))
+    return cudaErrorInvalidValue;
+  auto kern = paged_prefill_tc_kernel<Ty, D>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(tiles, a.num_kv_heads, a.num_seqs), kThreads, TcGeo<D>::kSmem, stream>>>(km, vm, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int block_size, long long num_slots) {
+  return block_size >= 8 && block_size <= 64 && num_slots <= 0x7fffffffll;
+}
+
+cudaError_t launch_prefill_tc(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
+                              cudaStream_t stream) {
+  if (bf16) {
+    return head_dim == 64 ? launch_tc<BF16, 64>(a, max_query_len, stream)
+                          : launch_tc<BF16, 128>(a, max_query_len, stream);
+  }
+  return head_dim == 64 ? launch_tc<F16, 64>(a, max_query_len, stream)
+                        : launch_tc<F16, 128>(a, max_query_len, stream);
+}
+
+}  // namespace pa

@@ -24,7 +24,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_decode_no_alloc_scratch_bytes", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
             "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
-            "pa_decode_append", "pa_prefill")
+            "pa_decode_append", "pa_prefill", "pa_wait_timeout_count")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -58,6 +58,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_last_error.restype = ctypes.c_char_p
     L.pa_bad_index_count.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
     L.pa_bad_index_count.restype = i32
+    L.pa_wait_timeout_count.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), i32]
+    L.pa_wait_timeout_count.restype = i32
     L.pa_decode_no_alloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                      ctypes.c_float, i32, i32, i32, i32, i32, vp]
     L.pa_decode_no_alloc.restype = i32
@@ -277,6 +279,13 @@ def bad_index_count(clear: bool = False) -> int:
     """Out-of-range indices the kernels skipped on the current device (synchronises)."""
     n = ctypes.c_ulonglong(0)
     _check(load_library().pa_bad_index_count(ctypes.byref(n), int(bool(clear))))
+    return int(n.value)
+
+
+def wait_timeout_count(clear: bool = False) -> int:
+    """Bounded in-kernel waits that gave up on the current device (synchronises); 0 when healthy."""
+    n = ctypes.c_ulonglong(0)
+    _check(load_library().pa_wait_timeout_count(ctypes.byref(n), int(bool(clear))))
     return int(n.value)
 
 

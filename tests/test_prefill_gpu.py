@@ -39,6 +39,7 @@ def _run(case, qlens, seed):
     ref = oracle.paged_prefill(q, case.key_cache, case.value_cache, case.block_tables, case.seq_lens,
                                starts, case.block_size, case.scale, case.dtype)
     check_parity(host_bits(out16), out32.cpu().numpy(), ref, case.dtype, f"prefill {case.name}")
+    assert pa.wait_timeout_count(clear=True) == 0
     return q, out32.cpu().numpy()
 
 
@@ -78,3 +79,36 @@ def test_long_prompt_many_tiles():
     case = W.random_case(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
                          len_range=(1500, 1500), dtype="bf16", seed=8)
     _run(case, [1500, 1000], 5)
+
+
+@pytest.mark.parametrize("B", [8, 16, 64, 2])
+def test_unused_slots_are_never_read(B):
+    # tail slots of each last block and blocks outside the tables hold NaN / Inf:
+    # the output must not change (rows past L are zero-filled, never loaded)
+    case = W.random_case(num_seqs=4, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=B,
+                         len_range=(3, 260), dtype="bf16", seed=30 + B)
+    qlens = [int(x) for x in np.minimum(case.seq_lens, 97)]
+    _, base = _run(case, qlens, 11)
+    W.poison_unused(case, W.nan_bits("bf16"))
+    _, nan_out = _run(case, qlens, 11)
+    W.poison_unused(case, W.inf_bits("bf16"))
+    _, inf_out = _run(case, qlens, 11)
+    assert np.array_equal(base, nan_out) and np.array_equal(base, inf_out)
+
+
+def test_bad_block_ids_are_counted_not_faulted():
+    case = W.random_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                         len_range=(100, 200), dtype="bf16", seed=41)
+    starts = np.array([0, 10, 20, 30], dtype=np.int32)
+    dc = DeviceCase(case)
+    bt = dc.block_tables.clone()
+    bt[1, 2] = case.num_blocks + 5   # inside sequence 1's length: read as zeros
+    bt[2, 0] = -3
+    q = dev_bits(W.normal_bits((30, 8, 128), "bf16", 5, 55), "bf16")
+    out = torch.empty((30, 8, 128), dtype=torch.float32, device="cuda")
+    pa.bad_index_count(clear=True)
+    pa.prefill(out, q, dc.key_cache, dc.value_cache, bt, dc.seq_lens, torch.from_numpy(starts).cuda(),
+               10, case.scale)
+    assert pa.bad_index_count(clear=True) >= 2
+    assert pa.wait_timeout_count(clear=True) == 0
+    assert torch.isfinite(out).all()
