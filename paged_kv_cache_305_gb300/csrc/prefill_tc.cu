@@ -70,15 +70,16 @@ static_assert(kStages == 2, "stage and S buffer of tile j are both j & 1");
 
 // barrier slots (8 bytes each) after the tiles
 enum : int {
-  kBarKFull = 0,   // [2]
-  kBarVFull = 2,   // [2]
-  kBarEmpty = 4,   // [2]
-  kBarSFull = 6,   // [2]
-  kBarPFull = 8,   // [2]
-  kBarODone = 10,
-  kBarQFull = 11,
-  kBarDone = 12,
-  kTmemSlot = 13,  // 4-byte TMEM base address
+  kBarKFull = 0,    // [2] K tile landed
+  kBarVFull = 2,    // [2] V tile landed
+  kBarKEmpty = 4,   // [2] S of the K tile done: stage reusable for K
+  kBarVEmpty = 6,   // [2] P V of the V tile done: stage reusable for V
+  kBarSFull = 8,    // [2] S in tensor memory
+  kBarPFull = 10,   // [2] weights (and any O rescale) in tensor memory
+  kBarODone = 12,   // P V done
+  kBarQFull = 13,   // query tile in shared memory
+  kBarDone = 14,    // every product of the CTA done
+  kTmemSlot = 15,   // 4-byte TMEM base address
 };
 
 // Offset of 16-byte chunk (chunk & 7) of row `row` inside one 128-byte-row
@@ -145,7 +146,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBarKFull + i), 1);
       tc::mbar_init(bar(kBarVFull + i), 1);
-      tc::mbar_init(bar(kBarEmpty + i), 1);
+      tc::mbar_init(bar(kBarKEmpty + i), 1);
+      tc::mbar_init(bar(kBarVEmpty + i), 1);
       tc::mbar_init(bar(kBarSFull + i), 1);
       tc::mbar_init(bar(kBarPFull + i), 128);
     }
@@ -172,6 +174,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const size_t row = static_cast<size_t>(q0 + j0 + jj) * a.num_q_heads +
                            static_cast<size_t>(h) * G + g;
         v = __ldg(reinterpret_cast<const uint4*>(qb + row * D) + c);
+        if (a.scale_log2 < 0.f) {  // q.k * scale == (-q).k * |scale|, exactly
+          v.x ^= 0x80008000u;
+          v.y ^= 0x80008000u;
+          v.z ^= 0x80008000u;
+          v.w ^= 0x80008000u;
+        }
       }
       st_shared_v4(sQ + (c >> 3) * Geo::kQHalf + sw_off(r, c), v);
     }
@@ -183,8 +191,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const bool row_valid = r < P * G && r / G < jn;
     const int qp = row_valid ? L - Q + j0 + r / G : last_pos;  // causal limit
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const float sl2 = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    const float sl2 = fabsf(a.scale_log2);  // the query tile carries the sign
+    float m = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of weights
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
       const uint32_t colS = static_cast<uint32_t>(b * kKeys);
@@ -210,15 +218,19 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           sv[48 + i] = __uint_as_float(x3[i]);
         }
       }
-      const int kb = j * kKeys;
-      float mx = -INFINITY;
+      // tokens kb + c with c > lim are past this row's causal limit
+      const int lim = qp - j * kKeys;
+      const bool diag = lim < kKeys - 1;
+      // row max of the raw scores, eight independent chains
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) {
-        const float x = kb + c <= qp ? sv[c] * sl2 : -INFINITY;
-        sv[c] = x;
-        mx = fmaxf(mx, x);
-      }
-      const float mn = fmaxf(m, mx);
+      for (int i = 0; i < 8; ++i) mx8[i] = diag && i > lim ? -INFINITY : sv[i];
+#pragma unroll
+      for (int c = 8; c < kKeys; ++c)
+        mx8[c & 7] = fmaxf(mx8[c & 7], diag && c > lim ? -INFINITY : sv[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
       if (__any_sync(kFull, mn > m + kRescaleLog2)) {
         const float alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
         if (j > 0) {
@@ -239,15 +251,23 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         l *= alpha;
         m = mn;
       }
-      float rs = 0.f;
+      // weights 2^(s*sl2 - m), written as a 16-bit head and the 16-bit
+      // rounding of the remainder; four partial sums
+      const float nm = -m;
+      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(sv[hh * 32 + 2 * i] - m);
-          const float p1 = ex2(sv[hh * 32 + 2 * i + 1] - m);
-          rs += p0 + p1;
+          const int c = hh * 32 + 2 * i;
+          float p0 = ex2(fmaf(sv[c], sl2, nm));
+          float p1 = ex2(fmaf(sv[c + 1], sl2, nm));
+          if (diag) {
+            p0 = c > lim ? 0.f : p0;
+            p1 = c + 1 > lim ? 0.f : p1;
+          }
+          rs4[i & 3] += p0 + p1;
           ph[i] = Ty::pack(p0, p1);
           const float2 d = Ty::unpack(ph[i]);
           pl[i] = Ty::pack(p0 - d.x, p1 - d.y);
@@ -255,6 +275,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tc::tmem_st16(lane_addr + colS + 16 * hh, ph);       // weights, head part
         tc::tmem_st16(lane_addr + colS + 32 + 16 * hh, pl);  // weights, remainder
       }
+      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
       l += rs;
       tc::tmem_st_wait();
       tc::tc_fence_before();
@@ -298,19 +319,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int B = 1 << shift;
     const int nb = kKeys >> shift;  // blocks per tile (1..8)
     const int32_t* trow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
-    const T* kc = static_cast<const T*>(a.key_cache);
-    const T* vc = static_cast<const T*>(a.value_cache);
     const size_t slot_stride = static_cast<size_t>(a.num_kv_heads) * D;
-    int j = 0;
-    for (; j < ntiles; ++j) {
-      const int st = j & 1;
-      if (j >= kStages) {
-        ok = warp_wait(bar(kBarEmpty + st), ((j >> 1) - 1) & 1);
-        if (!ok) break;
-      }
-      int id = -1, valid = 0;
-      if (lane < nb) {
-        const int blk = j * nb + lane;
+    // lane i < nb describes block i of a tile: its id (-1: none / out of
+    // range) and how many of its B tokens lie before L
+    auto block_of = [&](int jt, int& id, int& valid) {
+      id = -1;
+      valid = 0;
+      if (lane < nb && jt < ntiles) {
+        const int blk = jt * nb + lane;
         valid = min(max(L - (blk << shift), 0), B);
         if (valid > 0) {
           id = __ldg(trow + blk);
@@ -320,65 +336,91 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           }
         }
       }
-      const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
-      // blocks that are not whole and valid: copy their rows (zeros past L)
-      for (int i = 0; i < nb; ++i) {
-        const int idi = __shfl_sync(kFull, id, i);
-        const int vi = __shfl_sync(kFull, valid, i);
-        if ((whole >> i) & 1u) continue;
-        for (int idx = lane; idx < B * kChunks; idx += 32) {
-          const int t = idx / kChunks, c = idx % kChunks;
-          const int row = i * B + t;
-          uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
-          if (idi >= 0 && t < vi) {
-            const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
-                               static_cast<size_t>(h) * D + c * 8;
-            kv = __ldg(reinterpret_cast<const uint4*>(kc + off));
-            vv = __ldg(reinterpret_cast<const uint4*>(vc + off));
+    };
+    // one tensor (K or V) of tile j into stage st: rows of blocks that are
+    // not whole and valid by plain loads (zeros past L), whole blocks by TMA,
+    // one copy per lane (lane = block * halves + half)
+    auto fill = [&](const T* cache, const CUtensorMap* map, uint32_t dst0, uint32_t full_bar,
+                    int id, int valid, unsigned whole) {
+      if (whole != (1u << nb) - 1u) {
+        for (int i = 0; i < nb; ++i) {
+          const int idi = __shfl_sync(kFull, id, i);
+          const int vi = __shfl_sync(kFull, valid, i);
+          if ((whole >> i) & 1u) continue;
+          for (int idx = lane; idx < B * kChunks; idx += 32) {
+            const int t = idx / kChunks, c = idx % kChunks;
+            const int row = i * B + t;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (idi >= 0 && t < vi) {
+              const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
+                                 static_cast<size_t>(h) * D + c * 8;
+              v = __ldg(reinterpret_cast<const uint4*>(cache + off));
+            }
+            st_shared_v4(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(row, c), v);
           }
-          const uint32_t so = (c >> 3) * Geo::kTileHalf + sw_off(row, c);
-          st_shared_v4(sK(st) + so, kv);
-          st_shared_v4(sV(st) + so, vv);
         }
+        tc::fence_async_smem();
       }
-      tc::fence_async_smem();
       __syncwarp();
-      const uint32_t bytes = static_cast<uint32_t>(__popc(whole)) * B * D * 2;
-      if (lane == 0) {
-        tc::mbar_arrive_expect_tx(bar(kBarKFull + st), bytes);
-        tc::mbar_arrive_expect_tx(bar(kBarVFull + st), bytes);
+      if (lane == 0)
+        tc::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(__popc(whole)) * B * D * 2);
+      __syncwarp();
+      const int i = lane / Geo::kHalves, hf = lane % Geo::kHalves;
+      const int idi = __shfl_sync(kFull, id, i & 31);
+      if (i < nb && ((whole >> i) & 1u))
+        tc::tma_load_3d(dst0 + static_cast<uint32_t>(hf * Geo::kTileHalf + i * B * 128), map,
+                        full_bar, hf * 64, h, idi * B);
+    };
+    int id_n, valid_n;
+    block_of(0, id_n, valid_n);
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int st = j & 1;
+      const int id = id_n, valid = valid_n;
+      block_of(j + 1, id_n, valid_n);  // next tile's table entries, ahead of time
+      const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
+      if (j >= kStages) {
+        ok = warp_wait(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1);
+        if (!ok) break;
       }
-      for (int i = 0; i < nb; ++i) {
-        const int idi = __shfl_sync(kFull, id, i);
-        if (lane != 0 || !((whole >> i) & 1u)) continue;
-#pragma unroll
-        for (int hf = 0; hf < Geo::kHalves; ++hf) {
-          const uint32_t dst = static_cast<uint32_t>(hf * Geo::kTileHalf + i * B * 128);
-          tc::tma_load_3d(sK(st) + dst, &kmap, bar(kBarKFull + st), hf * 64, h, idi * B);
-          tc::tma_load_3d(sV(st) + dst, &vmap, bar(kBarVFull + st), hf * 64, h, idi * B);
-        }
+      fill(static_cast<const T*>(a.key_cache), &kmap, sK(st), bar(kBarKFull + st), id, valid, whole);
+      if (j >= kStages) {
+        ok = warp_wait(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1);
+        if (!ok) break;
       }
+      fill(static_cast<const T*>(a.value_cache), &vmap, sV(st), bar(kBarVFull + st), id, valid,
+           whole);
     }
     // copies still in flight (only after a wait gave up) must land before exit
-    for (int jj = max(0, j - kStages); jj < j; ++jj) {
+    for (int jj = max(0, j - kStages); jj <= j && jj < ntiles; ++jj) {
       tc::mbar_wait(bar(kBarKFull + (jj & 1)), (jj >> 1) & 1);
-      tc::mbar_wait(bar(kBarVFull + (jj & 1)), (jj >> 1) & 1);
+      if (jj < j) tc::mbar_wait(bar(kBarVFull + (jj & 1)), (jj >> 1) & 1);
     }
   } else if (warp == kMmaWarp && lane == 0) {
-    // ---------------- products, one thread
+    // ---------------- products, one thread; descriptors built once, moved by
+    // adding (byte offset >> 4) to the start-address field
     const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
     const uint32_t id_o = tc::idesc_f16(kRows, D, Ty::kIsBf16, true);
+    const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
+    const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
+    // V read MN-major: 8-token groups 1024 bytes apart (SBO), the two
+    // 64-element slices of the head dim kTileHalf apart (LBO)
+    const uint64_t dv0 = tc::sdesc_sw128(sV(0), Geo::kHalves > 1 ? Geo::kTileHalf : 16, 1024);
+    constexpr uint64_t kStageStep = Geo::kStageBytes >> 4;
+    auto kstep = [](int ks) {  // K-major: slice ks / 4, 32 bytes per 16 elements
+      return static_cast<uint64_t>(((ks >> 2) * Geo::kTileHalf + (ks & 3) * 32) >> 4);
+    };
     auto issue_s = [&](int j) {
       const int st = j & 1;
       const uint32_t d = tmem + static_cast<uint32_t>(st * kKeys);
+      const uint64_t dk = dk0 + st * kStageStep;
 #pragma unroll
       for (int ks = 0; ks < kKSteps; ++ks) {
-        const uint32_t koff = static_cast<uint32_t>((ks & 3) * 32);  // 16 elements = 32 bytes
-        const uint64_t da = tc::sdesc_sw128(sQ + (ks >> 2) * Geo::kQHalf + koff, 16, 1024);
-        const uint64_t db = tc::sdesc_sw128(sK(st) + (ks >> 2) * Geo::kTileHalf + koff, 16, 1024);
-        tc::mma_ss(d, da, db, id_s, ks > 0 ? 1u : 0u);
+        const uint64_t qoff = static_cast<uint64_t>(((ks >> 2) * Geo::kQHalf + (ks & 3) * 32) >> 4);
+        tc::mma_ss(d, dq0 + qoff, dk + kstep(ks), id_s, ks > 0 ? 1u : 0u);
       }
       tc::tc_commit(bar(kBarSFull + st));
+      tc::tc_commit(bar(kBarKEmpty + st));
     };
     ok = tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
     if (ok) {
@@ -400,20 +442,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       if (!ok) break;
       tc::tc_fence_after();
       const uint32_t colS = tmem + static_cast<uint32_t>(b * kKeys);
+      const uint64_t dv = dv0 + b * kStageStep;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {  // weights: head part, then remainder
 #pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks) {
-          // V read MN-major: 8-token groups 1024 bytes apart (SBO), the two
-          // 64-element slices of the head dim kTileHalf apart (LBO)
-          const uint64_t dv =
-              tc::sdesc_sw128(sV(b) + ks * 2048, Geo::kHalves > 1 ? Geo::kTileHalf : 16, 1024);
-          tc::mma_ts(tmem + kColO, colS + part * 32 + ks * 8, dv, id_o,
-                     (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          tc::mma_ts(tmem + kColO, colS + part * 32 + ks * 8, dv + static_cast<uint64_t>(ks * 128),
+                     id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
       }
       tc::tc_commit(bar(kBarODone));
-      tc::tc_commit(bar(kBarEmpty + b));
+      tc::tc_commit(bar(kBarVEmpty + b));
     }
     // nothing this thread issued may still be running when the CTA ends
     tc::tc_commit(bar(kBarDone));

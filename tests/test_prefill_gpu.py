@@ -25,7 +25,7 @@ def _cuda():
     torch.cuda.synchronize()
 
 
-def _run(case, qlens, seed):
+def _run(case, qlens, seed, scale=None):
     starts = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     q = W.normal_bits((int(starts[-1]), case.num_q_heads, case.head_dim), case.dtype, seed, 55)
     dc = DeviceCase(case)
@@ -34,10 +34,11 @@ def _run(case, qlens, seed):
     out16 = torch.empty_like(qd)
     out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
     mq = int(max(qlens))
-    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, case.scale)
-    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, case.scale)
+    sc = case.scale if scale is None else scale
+    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc)
+    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc)
     ref = oracle.paged_prefill(q, case.key_cache, case.value_cache, case.block_tables, case.seq_lens,
-                               starts, case.block_size, case.scale, case.dtype)
+                               starts, case.block_size, sc, case.dtype)
     check_parity(host_bits(out16), out32.cpu().numpy(), ref, case.dtype, f"prefill {case.name}")
     assert pa.wait_timeout_count(clear=True) == 0
     return q, out32.cpu().numpy()
@@ -112,3 +113,13 @@ def test_bad_block_ids_are_counted_not_faulted():
     assert pa.bad_index_count(clear=True) >= 2
     assert pa.wait_timeout_count(clear=True) == 0
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("B", [16, 4])
+@pytest.mark.parametrize("scale", [-0.3, 0.0, 1.5])
+def test_scale_sign_and_zero(B, scale):
+    # a negative scale flips which token dominates; zero gives the plain mean
+    # of the visible values
+    case = W.random_case(num_seqs=3, num_q_heads=8, num_kv_heads=4, head_dim=64, block_size=B,
+                         len_range=(20, 180), dtype="fp16", seed=50 + B)
+    _run(case, [int(x) for x in case.seq_lens], 12, scale=scale)
