@@ -561,7 +561,7 @@ def run_prefill(args):
     import paged_kv_cache_305_gb300 as pa
     from paged_kv_cache_305_gb300 import build as pbuild
     pbuild.build()
-    S, Hq, Hkv, d, B = 16, 32, 8, 128, 16
+    S, Hq, Hkv, d, B = 16, 32, 8, 128, args.prefill_block_size
     ctx, chunk = args.prefill_context, args.prefill_chunk
     case = W.random_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
                          len_range=(ctx, ctx), dtype="bf16", seed=0)
@@ -608,6 +608,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefill-context", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=2048)
+    ap.add_argument("--prefill-block-size", type=int, default=16)
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
                     help="fused: pa_decode_append; separate: pa_reshape_and_cache then pa_decode")
     ap.add_argument("--op", default="decode_step",

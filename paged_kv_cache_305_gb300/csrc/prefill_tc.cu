@@ -8,7 +8,7 @@
 // One CTA per (query tile, kv head, sequence). A query tile is 128 rows =
 // 128 / G positions x the G heads of the kv head (the product's M), so each
 // K/V tile serves every query head of the group. Key tiles are 64 tokens.
-// Roles (6 warps):
+// Roles (7 warps):
 //   warps 0-3  one thread per query row: loads the query tile, then for every
 //              key tile reads its row of S = q K^T from tensor memory, applies
 //              the causal limit, keeps the running max / sum (base 2), writes
@@ -16,11 +16,12 @@
 //              16-bit rounding of the remainder, and rescales its output row
 //              when the max has grown by more than 2^8 since the last rescale;
 //              finally divides by the sum and stores the row.
-//   warp 4     producer: whole blocks of the tile by TMA (one box per block
-//              and 64-element half of the head dim, straight from the block
+//   warps 4, 5 producers of the K and the V tiles (each on its own, so K
+//              runs ahead of V): whole blocks by TMA (one box per block and
+//              64-element half of the head dim, straight from the block
 //              table), partial / out-of-range blocks by plain loads with zero
-//              fill; two stages.
-//   warp 5     one thread issues the products: S_j = Q K_j^T (smem x smem,
+//              fill; two stages, a K stage reused as soon as its S is done.
+//   warp 6     one thread issues the products: S_j = Q K_j^T (smem x smem,
 //              M=128, N=64) into one of two S column ranges, and
 //              O += P_j V_j (weights from tensor memory, V from smem read
 //              MN-major, N = head dim) for the head and the remainder.
@@ -45,9 +46,10 @@ namespace {
 constexpr int kRows = 128;  // query rows per CTA = product M
 constexpr int kKeys = 64;   // tokens per key tile = N of S
 constexpr int kStages = 2;
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kThreads = 224;
+constexpr int kKWarp = 4;    // producer of K tiles
+constexpr int kVWarp = 5;    // producer of V tiles
+constexpr int kMmaWarp = 6;  // one thread issues the products
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColO = 128;
 constexpr float kRescaleLog2 = 8.f;
@@ -69,17 +71,18 @@ struct TcGeo {
 static_assert(kStages == 2, "stage and S buffer of tile j are both j & 1");
 
 // barrier slots (8 bytes each) after the tiles
+// Every batch of products is followed by exactly one tcgen05.commit, on one
+// barrier; whoever needs that batch finished waits on that barrier (the K
+// producer on S, the V producer on P V), so nothing depends on how a commit
+// relates to earlier ones.
 enum : int {
-  kBarKFull = 0,    // [2] K tile landed
-  kBarVFull = 2,    // [2] V tile landed
-  kBarKEmpty = 4,   // [2] S of the K tile done: stage reusable for K
-  kBarVEmpty = 6,   // [2] P V of the V tile done: stage reusable for V
-  kBarSFull = 8,    // [2] S in tensor memory
-  kBarPFull = 10,   // [2] weights (and any O rescale) in tensor memory
-  kBarODone = 12,   // P V done
-  kBarQFull = 13,   // query tile in shared memory
-  kBarDone = 14,    // every product of the CTA done
-  kTmemSlot = 15,   // 4-byte TMEM base address
+  kBarKFull = 0,   // [2] K tile landed
+  kBarVFull = 2,   // [2] V tile landed
+  kBarSFull = 4,   // [2] S_j done: S in tensor memory, K stage free
+  kBarPFull = 6,   // [2] weights (and any O rescale) in tensor memory
+  kBarODone = 8,   // [2] P_j V done: O updated, V stage and S columns free
+  kBarQFull = 10,  // query tile in shared memory
+  kTmemSlot = 11,  // 4-byte TMEM base address
 };
 
 // Offset of 16-byte chunk (chunk & 7) of row `row` inside one 128-byte-row
@@ -146,14 +149,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(bar(kBarKFull + i), 1);
       tc::mbar_init(bar(kBarVFull + i), 1);
-      tc::mbar_init(bar(kBarKEmpty + i), 1);
-      tc::mbar_init(bar(kBarVEmpty + i), 1);
       tc::mbar_init(bar(kBarSFull + i), 1);
       tc::mbar_init(bar(kBarPFull + i), 128);
+      tc::mbar_init(bar(kBarODone + i), 1);
     }
-    tc::mbar_init(bar(kBarODone), 1);
     tc::mbar_init(bar(kBarQFull), 128);
-    tc::mbar_init(bar(kBarDone), 1);
     tc::mbar_init_fence();
   }
   if (warp == 0) tc::tmem_alloc(bar(kTmemSlot), kTmemCols);
@@ -235,7 +235,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const float alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
         if (j > 0) {
           // the previous tile's P V must have landed before O is rescaled
-          ok = warp_wait(bar(kBarODone), (j - 1) & 1);
+          ok = warp_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
           if (!ok) break;
           tc::tc_fence_after();
 #pragma unroll
@@ -281,7 +281,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       tc::tc_fence_before();
       tc::mbar_arrive(bar(kBarPFull + b));
     }
-    if (ok) ok = warp_wait(bar(kBarODone), (ntiles - 1) & 1);
+    if (ok) ok = warp_wait(bar(kBarODone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
     if (ok) {
       tc::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -314,8 +314,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         }
       }
     }
-  } else if (warp == kProducerWarp) {
-    // ---------------- producer: K and V tiles of 64 tokens through the block table
+  } else if (warp == kKWarp || warp == kVWarp) {
+    // ---------------- producers: K (or V) tiles of 64 tokens through the block table
+    const bool is_v = warp == kVWarp;
+    const T* cache = static_cast<const T*>(is_v ? a.value_cache : a.key_cache);
+    const CUtensorMap* map = is_v ? &vmap : &kmap;
+    const int full0 = is_v ? kBarVFull : kBarKFull;
+    const int empty0 = is_v ? kBarODone : kBarSFull;  // stage free once S_j / P_j V is done
+    if (lane == 0) tc::prefetch_tensormap(map);
     const int B = 1 << shift;
     const int nb = kKeys >> shift;  // blocks per tile (1..8)
     const int32_t* trow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
@@ -331,7 +337,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (valid > 0) {
           id = __ldg(trow + blk);
           if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-            atomicAdd(a.bad, 1ull);
+            if (!is_v) atomicAdd(a.bad, 1ull);  // counted once, by the K producer
             id = -1;
           }
         }
@@ -380,22 +386,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       block_of(j + 1, id_n, valid_n);  // next tile's table entries, ahead of time
       const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
       if (j >= kStages) {
-        ok = warp_wait(bar(kBarKEmpty + st), ((j >> 1) - 1) & 1);
+        ok = warp_wait(bar(empty0 + st), ((j >> 1) - 1) & 1);
         if (!ok) break;
       }
-      fill(static_cast<const T*>(a.key_cache), &kmap, sK(st), bar(kBarKFull + st), id, valid, whole);
-      if (j >= kStages) {
-        ok = warp_wait(bar(kBarVEmpty + st), ((j >> 1) - 1) & 1);
-        if (!ok) break;
-      }
-      fill(static_cast<const T*>(a.value_cache), &vmap, sV(st), bar(kBarVFull + st), id, valid,
-           whole);
+      fill(cache, map, is_v ? sV(st) : sK(st), bar(full0 + st), id, valid, whole);
     }
     // copies still in flight (only after a wait gave up) must land before exit
-    for (int jj = max(0, j - kStages); jj <= j && jj < ntiles; ++jj) {
-      tc::mbar_wait(bar(kBarKFull + (jj & 1)), (jj >> 1) & 1);
-      if (jj < j) tc::mbar_wait(bar(kBarVFull + (jj & 1)), (jj >> 1) & 1);
-    }
+    for (int jj = max(0, j - kStages); jj < j; ++jj)
+      tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
   } else if (warp == kMmaWarp && lane == 0) {
     // ---------------- products, one thread; descriptors built once, moved by
     // adding (byte offset >> 4) to the start-address field
@@ -420,22 +418,26 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tc::mma_ss(d, dq0 + qoff, dk + kstep(ks), id_s, ks > 0 ? 1u : 0u);
       }
       tc::tc_commit(bar(kBarSFull + st));
-      tc::tc_commit(bar(kBarKEmpty + st));
     };
+    uint32_t last_bar = 0, last_parity = 0;  // the latest commit
     ok = tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
     if (ok) {
       tc::tc_fence_after();
       issue_s(0);
+      last_bar = bar(kBarSFull);
+      last_parity = 0;
     }
     for (int j = 0; j < ntiles && ok; ++j) {
       const int b = j & 1;
       if (j + 1 < ntiles) {
         // S_{j+1} overwrites the columns that held P_{j-1}: wait for P_{j-1} V
-        if (j >= 1) ok = tc::mbar_wait(bar(kBarODone), (j - 1) & 1);
+        if (j >= 1) ok = tc::mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
         if (ok) ok = tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
         if (!ok) break;
         tc::tc_fence_after();
         issue_s(j + 1);
+        last_bar = bar(kBarSFull + ((j + 1) & 1));
+        last_parity = ((j + 1) >> 1) & 1;
       }
       ok = tc::mbar_wait(bar(kBarPFull + b), (j >> 1) & 1) &&
            tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
@@ -450,12 +452,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           tc::mma_ts(tmem + kColO, colS + part * 32 + ks * 8, dv + static_cast<uint64_t>(ks * 128),
                      id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
       }
-      tc::tc_commit(bar(kBarODone));
-      tc::tc_commit(bar(kBarVEmpty + b));
+      tc::tc_commit(bar(kBarODone + b));
+      last_bar = bar(kBarODone + b);
+      last_parity = (j >> 1) & 1;
     }
     // nothing this thread issued may still be running when the CTA ends
-    tc::tc_commit(bar(kBarDone));
-    tc::mbar_wait(bar(kBarDone), 0);
+    if (last_bar != 0) tc::mbar_wait(last_bar, last_parity);
   }
 
   if (!ok && lane == 0) atomicAdd(a.timeouts, 1ull);

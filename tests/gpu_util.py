@@ -79,8 +79,13 @@ def check_parity(out16: np.ndarray, out32: np.ndarray, ref: np.ndarray, dtype: s
     """
     o32 = np.asarray(out32, dtype=np.float64)
     assert np.all(np.isfinite(o32)), f"{what}: non-finite output"
-    err = float(np.max(np.abs(o32 - ref))) if ref.size else 0.0
-    assert err <= ATOL, f"{what}: max |fp32 - oracle| = {err}"
+    diff = np.abs(o32 - ref)
+    err = float(np.max(diff)) if ref.size else 0.0
+    if err > ATOL:
+        where = np.unravel_index(int(np.argmax(diff)), diff.shape)
+        rows = np.argwhere(diff.reshape(diff.shape[0], -1).max(axis=1) > ATOL).ravel()
+        raise AssertionError(f"{what}: max |fp32 - oracle| = {err} at {tuple(int(x) for x in where)}; "
+                             f"{len(rows)} rows above tolerance, first {rows[:12].tolist()}")
     rounded = oracle.round_to_dtype(o32, dtype)
     bad = int(np.sum(rounded != out16))
     assert bad == 0, f"{what}: {bad} 16-bit outputs differ from the rounding of the fp32 result"
