@@ -97,6 +97,40 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+// Packed pairs of fp32 (one 64-bit register) and the paired fp32 operations
+// of sm_100-family cores, plus the three-input max: fewer instructions in the
+// per-row softmax.
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Bounded wait made uniform across the warp: every lane of a warp that
 // executes warp-collective tensor-memory instructions must take the same path.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
@@ -221,15 +255,21 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       // tokens kb + c with c > lim are past this row's causal limit
       const int lim = qp - j * kKeys;
       const bool diag = lim < kKeys - 1;
-      // row max of the raw scores, eight independent chains
-      float mx8[8];
+      if (diag) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx8[i] = diag && i > lim ? -INFINITY : sv[i];
+        for (int c = 0; c < kKeys; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
+      }
+      // row max of the raw scores: four chains of three-input maxima
+      float mx4[4];
 #pragma unroll
-      for (int c = 8; c < kKeys; ++c)
-        mx8[c & 7] = fmaxf(mx8[c & 7], diag && c > lim ? -INFINITY : sv[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float* v = sv + 16 * q4;
+        float mq = max3(v[0], v[1], v[2]);
+#pragma unroll
+        for (int c = 3; c < 15; c += 2) mq = max3(mq, v[c], v[c + 1]);
+        mx4[q4] = fmaxf(mq, v[15]);
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
       if (__any_sync(kFull, mn > m + kRescaleLog2)) {
         const float alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
@@ -252,30 +292,33 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         m = mn;
       }
       // weights 2^(s*sl2 - m), written as a 16-bit head and the 16-bit
-      // rounding of the remainder; four partial sums
-      const float nm = -m;
-      float rs4[4] = {0.f, 0.f, 0.f, 0.f};
+      // rounding of the remainder; paired fp32 arithmetic, four partial sums
+      const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int c = hh * 32 + 2 * i;
-          float p0 = ex2(fmaf(sv[c], sl2, nm));
-          float p1 = ex2(fmaf(sv[c + 1], sl2, nm));
-          if (diag) {
+          const float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
+          float p0 = ex2(arg.x), p1 = ex2(arg.y);
+          if (diag) {  // exact zeros past the limit (also for a zero scale)
             p0 = c > lim ? 0.f : p0;
             p1 = c + 1 > lim ? 0.f : p1;
           }
-          rs4[i & 3] += p0 + p1;
+          const uint64_t pp = f2(p0, p1);
+          rs2[i & 3] = f2_add(rs2[i & 3], pp);
           ph[i] = Ty::pack(p0, p1);
           const float2 d = Ty::unpack(ph[i]);
-          pl[i] = Ty::pack(p0 - d.x, p1 - d.y);
+          const float2 r = f2_split(f2_sub(pp, f2(d.x, d.y)));
+          pl[i] = Ty::pack(r.x, r.y);
         }
         tc::tmem_st16(lane_addr + colS + 16 * hh, ph);       // weights, head part
         tc::tmem_st16(lane_addr + colS + 32 + 16 * hh, pl);  // weights, remainder
       }
-      const float rs = (rs4[0] + rs4[1]) + (rs4[2] + rs4[3]);
+      const float2 ra = f2_split(f2_add(rs2[0], rs2[1])), rb = f2_split(f2_add(rs2[2], rs2[3]));
+      const float rs = (ra.x + ra.y) + (rb.x + rb.y);
       l += rs;
       tc::tmem_st_wait();
       tc::tc_fence_before();
