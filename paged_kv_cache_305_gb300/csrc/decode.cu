@@ -98,7 +98,10 @@ __device__ __forceinline__ long long first_pos(int c, int C, long long W) {
   return static_cast<long long>(c) * q + (static_cast<long long>(c) * r + C - 1) / C;
 }
 
-template <typename Ty, int D, int STAGES, int NT>
+// APPEND: the step's new K/V rows are given (pa_decode_append): the tile
+// holding each sequence's newest token reads that row from them and stores
+// it into its cache slot. Without it the kernel carries none of that code.
+template <typename Ty, int D, int STAGES, int NT, bool APPEND>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
 paged_decode_kernel(const DecodeArgs a) {
   using Geo = Geometry<D, STAGES>;
@@ -136,7 +139,6 @@ paged_decode_kernel(const DecodeArgs a) {
   Seg* sSeg = reinterpret_cast<Seg*>(sML + kWarps * 2 * kRows);
   float* sMerge =  // [warp][G][kOS], present only when warps share a head
       reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(sSeg) + Geo::kSegBytes);
-  __shared__ int sFresh[kWarps][STAGES];  // per ring slot: block id of the newest token's row, or -1
   __shared__ long long sW[3];  // base position of the first / last unit's row
   __shared__ int sRange[6];    // first unit (hg, s, p), end unit (hg, s, p)
 
@@ -351,12 +353,12 @@ paged_decode_kernel(const DecodeArgs a) {
         const size_t hoff = static_cast<size_t>(h) * D + cc * 8;
         const T* kb = kcache + hoff;
         const T* vb = vcache + hoff;
-        // with new K/V given, the tile holding the sequence's newest token reads
-        // that row from them (and the compute step stores it into its slot)
-        const int fresh_r = (a.new_key != nullptr && g.t1 == g.L) ? g.L - 1 - tb : -1;
-        const size_t nrow = (static_cast<size_t>(g.s) * Hkv + h) * D + cc * 8;
-#pragma unroll
-        for (int i = 0; i < kCopies; ++i) {
+        // with new K/V given, the one tile holding the sequence's newest token
+        // (warp-uniform test) reads that row from them; the compute step then
+        // stores it into its slot
+        const bool fresh_tile = APPEND && g.t1 == g.L && tb + kTileTokens >= g.L;
+        const int fresh_r = fresh_tile ? g.L - 1 - tb : -1;
+        auto copy = [&](int i, bool check_fresh) {
           const int r = cr + i * kRowsPerCopy;
           const int phys = __shfl_sync(kFull, idq[0], r);
           const int t = tb + r;
@@ -365,20 +367,21 @@ paged_decode_kernel(const DecodeArgs a) {
           if (in && !ok && cc == 0) atomicAdd(a.bad, 1ull);  // rejected id: its rows read as zero
           const size_t slot = ok ? (static_cast<size_t>(phys) << shift) + (t & bmask) : 0;
           const uint32_t off = r * kRowBytes + swz(r, cc);
-          if (r == fresh_r) {
+          if (check_fresh && r == fresh_r) {
+            const size_t nrow = (static_cast<size_t>(g.s) * Hkv + h) * D + cc * 8;
             cp_async_16(smem_u32(sk + off), static_cast<const T*>(a.new_key) + nrow, true);
             cp_async_16(smem_u32(sv + off), static_cast<const T*>(a.new_value) + nrow, true);
           } else {
             cp_async_16(smem_u32(sk + off), kb + slot * slot_stride, ok);
             cp_async_16(smem_u32(sv + off), vb + slot * slot_stride, ok);
           }
-        }
-        {
-          const int fp = __shfl_sync(kFull, idq[0], fresh_r >= 0 && fresh_r < kTileTokens ? fresh_r : 0);
-          if (lane == 0)
-            sFresh[warp][issued % STAGES] =
-                (fresh_r >= 0 && fresh_r < kTileTokens &&
-                 static_cast<unsigned>(fp) < static_cast<unsigned>(a.num_blocks)) ? fp : -1;
+        };
+        if (fresh_tile) {
+#pragma unroll
+          for (int i = 0; i < kCopies; ++i) copy(i, true);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kCopies; ++i) copy(i, false);
         }
         ++issued;
         advance(is_sg, is_j);
@@ -405,17 +408,22 @@ paged_decode_kernel(const DecodeArgs a) {
         __syncwarp();
         const unsigned char* sk = wpipe + (consumed % STAGES) * Geo::kStageBytes;
         const unsigned char* sv = sk + Geo::kTileBytes;
-        const int fresh_phys = sFresh[warp][consumed % STAGES];
         ++consumed;
         const int valid = g.t1 - (g.t0 + j * kTileTokens);  // >= 1
-        if (fresh_phys >= 0 && lane < kChunks) {
-          // the step's new K/V row, now in shared memory, goes to its cache slot
-          const int r = g.L - 1 - (g.t0 + j * kTileTokens);
-          const size_t dst = ((static_cast<size_t>(fresh_phys) << shift) + ((g.L - 1) & bmask)) * slot_stride +
-                             static_cast<size_t>(g.hg * Hc + hi) * D + lane * 8;
-          const uint32_t off = r * kRowBytes + swz(r, lane);
-          *reinterpret_cast<uint4*>(const_cast<T*>(kcache) + dst) = *reinterpret_cast<const uint4*>(sk + off);
-          *reinterpret_cast<uint4*>(const_cast<T*>(vcache) + dst) = *reinterpret_cast<const uint4*>(sv + off);
+        if (APPEND && g.t1 == g.L && valid <= kTileTokens && lane < kChunks) {
+          // the tile holds the newest token: its row (from the new K/V, now in
+          // shared memory) goes to its cache slot; a rejected block id stores
+          // nothing (already counted when the tile was loaded)
+          const int fresh_phys = __ldg(a.block_tables + static_cast<size_t>(g.s) * a.max_blocks_per_seq +
+                                       ((g.L - 1) >> shift));
+          if (static_cast<unsigned>(fresh_phys) < static_cast<unsigned>(a.num_blocks)) {
+            const int r = valid - 1;
+            const size_t dst = ((static_cast<size_t>(fresh_phys) << shift) + ((g.L - 1) & bmask)) * slot_stride +
+                               static_cast<size_t>(g.hg * Hc + hi) * D + lane * 8;
+            const uint32_t off = r * kRowBytes + swz(r, lane);
+            *reinterpret_cast<uint4*>(const_cast<T*>(kcache) + dst) = *reinterpret_cast<const uint4*>(sk + off);
+            *reinterpret_cast<uint4*>(const_cast<T*>(vcache) + dst) = *reinterpret_cast<const uint4*>(sv + off);
+          }
         }
 
         // scores S^T[token][head] = K q^T: 16 tokens x 8*NT heads. The k-steps
@@ -693,7 +701,7 @@ paged_decode_kernel(const DecodeArgs a) {
   }
 }
 
-template <typename Ty, int D, int STAGES, int NT>
+template <typename Ty, int D, int STAGES, int NT, bool APPEND>
 cudaError_t plan_typed(const DecodeArgs& a, int* ctas_per_sm, size_t* smem) {
   const int warps_per_head = kWarps / a.heads_per_cta;
   const size_t merge = warps_per_head > 1 ? static_cast<size_t>(kWarps) * a.group *
@@ -704,7 +712,7 @@ cudaError_t plan_typed(const DecodeArgs& a, int* ctas_per_sm, size_t* smem) {
   // to the largest request (a full merge area for 16 query heads)
   const size_t most = static_cast<size_t>(Geometry<D, STAGES>::kFixedBytes) +
                       static_cast<size_t>(kWarps) * kMaxGroup * Geometry<D, STAGES>::kOStride * 4;
-  auto kern = paged_decode_kernel<Ty, D, STAGES, NT>;
+  auto kern = paged_decode_kernel<Ty, D, STAGES, NT, APPEND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(most));
   if (e != cudaSuccess) return e;
@@ -716,9 +724,9 @@ cudaError_t plan_typed(const DecodeArgs& a, int* ctas_per_sm, size_t* smem) {
   return cudaSuccess;
 }
 
-template <typename Ty, int D, int STAGES, int NT>
+template <typename Ty, int D, int STAGES, int NT, bool APPEND>
 cudaError_t launch_typed(const DecodeArgs& a, long long grid, size_t smem, cudaStream_t stream) {
-  paged_decode_kernel<Ty, D, STAGES, NT>
+  paged_decode_kernel<Ty, D, STAGES, NT, APPEND>
       <<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
@@ -726,25 +734,25 @@ cudaError_t launch_typed(const DecodeArgs& a, long long grid, size_t smem, cudaS
 // Launch plans (ring depth, CTAs per SM, shared memory) cached per device
 // and kernel variant, so the occupancy query runs once, not on every call.
 constexpr int kPlanDevices = 64;
-constexpr int kPlanSlots = 2 * 2 * 2 * (kMaxGroup + 1) * 3;
+constexpr int kPlanSlots = 2 * 2 * 2 * 2 * (kMaxGroup + 1) * 3;
 std::atomic<unsigned long long> g_plans[kPlanDevices][kPlanSlots];
 
-template <typename Ty, int D, int NT>
+template <typename Ty, int D, int NT, bool APPEND>
 cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   const int hc_slot = a.heads_per_cta == 4 ? 2 : (a.heads_per_cta == 2 ? 1 : 0);
-  const int slot = (((Ty::kIsBf16 ? 1 : 0) * 2 + (D == 128 ? 1 : 0)) * 2 +
+  const int slot = ((((APPEND ? 1 : 0) * 2 + (Ty::kIsBf16 ? 1 : 0)) * 2 + (D == 128 ? 1 : 0)) * 2 +
                     (NT - 1)) * (kMaxGroup + 1) * 3 + a.group * 3 + hc_slot;
   unsigned long long plan = (dev >= 0 && dev < kPlanDevices) ? g_plans[dev][slot].load() : 0ull;
   if (plan == 0) {
     // the ring depth that fits the most CTAs on an SM (three stages on a tie)
     int n3 = 0, n2 = 0;
     size_t m3 = 0, m2 = 0;
-    e = plan_typed<Ty, D, 3, NT>(a, &n3, &m3);
+    e = plan_typed<Ty, D, 3, NT, APPEND>(a, &n3, &m3);
     if (e != cudaSuccess) return e;
-    e = plan_typed<Ty, D, 2, NT>(a, &n2, &m2);
+    e = plan_typed<Ty, D, 2, NT, APPEND>(a, &n2, &m2);
     if (e != cudaSuccess) return e;
     const bool three = n3 >= n2;
     const unsigned long long per = static_cast<unsigned long long>(three ? n3 : n2);
@@ -761,14 +769,17 @@ cudaError_t launch_d(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
                           (a.num_kv_heads / a.heads_per_cta) * a.max_partitions;
   if (grid > units) grid = units;
   if (grid < 1) grid = 1;
-  return three ? launch_typed<Ty, D, 3, NT>(a, grid, smem, stream)
-               : launch_typed<Ty, D, 2, NT>(a, grid, smem, stream);
+  return three ? launch_typed<Ty, D, 3, NT, APPEND>(a, grid, smem, stream)
+               : launch_typed<Ty, D, 2, NT, APPEND>(a, grid, smem, stream);
 }
 
 template <typename Ty, int D>
 cudaError_t launch_g(const DecodeArgs& a, int num_sms, cudaStream_t stream) {
-  return a.group <= 8 ? launch_d<Ty, D, 1>(a, num_sms, stream)
-                      : launch_d<Ty, D, 2>(a, num_sms, stream);
+  if (a.new_key != nullptr)
+    return a.group <= 8 ? launch_d<Ty, D, 1, true>(a, num_sms, stream)
+                        : launch_d<Ty, D, 2, true>(a, num_sms, stream);
+  return a.group <= 8 ? launch_d<Ty, D, 1, false>(a, num_sms, stream)
+                      : launch_d<Ty, D, 2, false>(a, num_sms, stream);
 }
 
 }  // namespace
