@@ -10,24 +10,25 @@
 // K/V tile serves every query head of the group. Key tiles are 64 tokens.
 // Roles (7 warps):
 //   warps 0-3  one thread per query row: loads the query tile, then for every
-//              key tile reads its row of S = q K^T from tensor memory, applies
+//              key tile reads its row of S = q K^T from tensor memory (and at
+//              once frees the S columns for the next tile's product), applies
 //              the causal limit, keeps the running max / sum (base 2), writes
-//              the weights back into tensor memory as a 16-bit head plus the
-//              16-bit rounding of the remainder, and rescales its output row
-//              when the max has grown by more than 2^8 since the last rescale;
-//              finally divides by the sum and stores the row.
+//              the weights into tensor memory as a 16-bit head plus the 16-bit
+//              rounding of the remainder, and rescales its output row when the
+//              max has grown by more than 2^8 since the last rescale; finally
+//              divides by the sum and stores the row.
 //   warps 4, 5 producers of the K and the V tiles (each on its own, so K
 //              runs ahead of V): whole blocks by TMA (one box per block and
 //              64-element half of the head dim, straight from the block
 //              table), partial / out-of-range blocks by plain loads with zero
 //              fill; two stages, a K stage reused as soon as its S is done.
-//   warp 6     one thread issues the products: S_j = Q K_j^T (smem x smem,
-//              M=128, N=64) into one of two S column ranges, and
+//   warp 6     one thread issues the products: S_{j+1} = Q K_{j+1}^T (smem x
+//              smem, M=128, N=64) as soon as the softmax has read S_j, and
 //              O += P_j V_j (weights from tensor memory, V from smem read
 //              MN-major, N = head dim) for the head and the remainder.
-// Tensor memory (256 columns): S0 at 0, S1 at 64 (each later overwritten by
-// its weights), O at 128. All waits are bounded; a wait that gives up is
-// counted and the CTA winds down without hanging.
+// Tensor memory (256 columns): S at 0, P at 64, O at 128, so the product of
+// the next S overlaps the whole softmax of the current tile. All waits are
+// bounded; a wait that gives up is counted and the CTA winds down.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -51,7 +52,9 @@ constexpr int kKWarp = 4;    // producer of K tiles
 constexpr int kVWarp = 5;    // producer of V tiles
 constexpr int kMmaWarp = 6;  // one thread issues the products
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kColS = 0;    // S, 64 fp32 columns
+constexpr uint32_t kColP = 64;   // P: 32 columns of packed 16-bit heads, 32 of remainders
+constexpr uint32_t kColO = 128;  // O, head_dim fp32 columns
 constexpr float kRescaleLog2 = 8.f;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -75,12 +78,15 @@ static_assert(kStages == 2, "stage and S buffer of tile j are both j & 1");
 // barrier; whoever needs that batch finished waits on that barrier (the K
 // producer on S, the V producer on P V), so nothing depends on how a commit
 // relates to earlier ones.
+// Barriers that a waiter could otherwise see two phases ahead are kept per
+// tile parity ([2]).
 enum : int {
   kBarKFull = 0,   // [2] K tile landed
   kBarVFull = 2,   // [2] V tile landed
   kBarSFull = 4,   // [2] S_j done: S in tensor memory, K stage free
-  kBarPFull = 6,   // [2] weights (and any O rescale) in tensor memory
-  kBarODone = 8,   // [2] P_j V done: O updated, V stage and S columns free
+  kBarPFull = 6,   // weights P_j (and any O rescale) in tensor memory
+  kBarSFree = 7,   // S_j read into registers: the S columns may be overwritten
+  kBarODone = 8,   // [2] P_j V done: O updated, V stage and P columns free
   kBarQFull = 10,  // query tile in shared memory
   kTmemSlot = 11,  // 4-byte TMEM base address
 };
@@ -184,9 +190,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       tc::mbar_init(bar(kBarKFull + i), 1);
       tc::mbar_init(bar(kBarVFull + i), 1);
       tc::mbar_init(bar(kBarSFull + i), 1);
-      tc::mbar_init(bar(kBarPFull + i), 128);
       tc::mbar_init(bar(kBarODone + i), 1);
     }
+    tc::mbar_init(bar(kBarPFull), 128);
+    tc::mbar_init(bar(kBarSFree), 128);
     tc::mbar_init(bar(kBarQFull), 128);
     tc::mbar_init_fence();
   }
@@ -228,18 +235,16 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const float sl2 = fabsf(a.scale_log2);  // the query tile carries the sign
     float m = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of weights
     for (int j = 0; j < ntiles; ++j) {
-      const int b = j & 1;
-      const uint32_t colS = static_cast<uint32_t>(b * kKeys);
-      ok = warp_wait(bar(kBarSFull + b), (j >> 1) & 1);
+      ok = warp_wait(bar(kBarSFull + (j & 1)), (j >> 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
       float sv[kKeys];
       {
         uint32_t x0[16], x1[16], x2[16], x3[16];
-        tc::tmem_ld16(lane_addr + colS, x0);
-        tc::tmem_ld16(lane_addr + colS + 16, x1);
-        tc::tmem_ld16(lane_addr + colS + 32, x2);
-        tc::tmem_ld16(lane_addr + colS + 48, x3);
+        tc::tmem_ld16(lane_addr + kColS, x0);
+        tc::tmem_ld16(lane_addr + kColS + 16, x1);
+        tc::tmem_ld16(lane_addr + kColS + 32, x2);
+        tc::tmem_ld16(lane_addr + kColS + 48, x3);
         tc::tmem_ld_wait16(x0);
         tc::tmem_ld_wait16(x1);
         tc::tmem_ld_wait16(x2);
@@ -252,6 +257,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           sv[48 + i] = __uint_as_float(x3[i]);
         }
       }
+      // S_j is in registers: S_{j+1} may now be written into the same columns
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kBarSFree));
       // tokens kb + c with c > lim are past this row's causal limit
       const int lim = qp - j * kKeys;
       const bool diag = lim < kKeys - 1;
@@ -271,13 +279,42 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
-      if (__any_sync(kFull, mn > m + kRescaleLog2)) {
-        const float alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
-        if (j > 0) {
-          // the previous tile's P V must have landed before O is rescaled
-          ok = warp_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
-          if (!ok) break;
-          tc::tc_fence_after();
+      const bool rescale = __any_sync(kFull, mn > m + kRescaleLog2);
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
+        l *= alpha;
+        m = mn;
+      }
+      // weights 2^(s*sl2 - m) as a 16-bit head and the 16-bit rounding of the
+      // remainder, held in registers; paired fp32 arithmetic, four partial sums
+      const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
+      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+      uint32_t ph[32], pl[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int c = 2 * i;
+        const float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
+        float p0 = ex2(arg.x), p1 = ex2(arg.y);
+        if (diag) {  // exact zeros past the limit (also for a zero scale)
+          p0 = c > lim ? 0.f : p0;
+          p1 = c + 1 > lim ? 0.f : p1;
+        }
+        const uint64_t pp = f2(p0, p1);
+        rs2[i & 3] = f2_add(rs2[i & 3], pp);
+        ph[i] = Ty::pack(p0, p1);
+        const float2 d = Ty::unpack(ph[i]);
+        const float2 r = f2_split(f2_sub(pp, f2(d.x, d.y)));
+        pl[i] = Ty::pack(r.x, r.y);
+      }
+      const float2 ra = f2_split(f2_add(rs2[0], rs2[1])), rb = f2_split(f2_add(rs2[2], rs2[3]));
+      l += (ra.x + ra.y) + (rb.x + rb.y);
+      if (j > 0) {
+        // P_{j-1} V must be done before P_j overwrites its columns and O is rescaled
+        ok = warp_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
+        if (!ok) break;
+        tc::tc_fence_after();
+        if (rescale) {
 #pragma unroll
           for (int c = 0; c < D / 16; ++c) {
             uint32_t x[16];
@@ -288,41 +325,22 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             tc::tmem_st16(lane_addr + kColO + 16 * c, x);
           }
         }
-        l *= alpha;
-        m = mn;
       }
-      // weights 2^(s*sl2 - m), written as a 16-bit head and the 16-bit
-      // rounding of the remainder; paired fp32 arithmetic, four partial sums
-      const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
-      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
+      {
+        uint32_t w[16];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t ph[16], pl[16];
+        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = hh * 32 + 2 * i;
-          const float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
-          float p0 = ex2(arg.x), p1 = ex2(arg.y);
-          if (diag) {  // exact zeros past the limit (also for a zero scale)
-            p0 = c > lim ? 0.f : p0;
-            p1 = c + 1 > lim ? 0.f : p1;
-          }
-          const uint64_t pp = f2(p0, p1);
-          rs2[i & 3] = f2_add(rs2[i & 3], pp);
-          ph[i] = Ty::pack(p0, p1);
-          const float2 d = Ty::unpack(ph[i]);
-          const float2 r = f2_split(f2_sub(pp, f2(d.x, d.y)));
-          pl[i] = Ty::pack(r.x, r.y);
+          for (int i = 0; i < 16; ++i) w[i] = ph[16 * hh + i];
+          tc::tmem_st16(lane_addr + kColP + 16 * hh, w);       // weights, head part
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = pl[16 * hh + i];
+          tc::tmem_st16(lane_addr + kColP + 32 + 16 * hh, w);  // weights, remainder
         }
-        tc::tmem_st16(lane_addr + colS + 16 * hh, ph);       // weights, head part
-        tc::tmem_st16(lane_addr + colS + 32 + 16 * hh, pl);  // weights, remainder
       }
-      const float2 ra = f2_split(f2_add(rs2[0], rs2[1])), rb = f2_split(f2_add(rs2[2], rs2[3]));
-      const float rs = (ra.x + ra.y) + (rb.x + rb.y);
-      l += rs;
       tc::tmem_st_wait();
       tc::tc_fence_before();
-      tc::mbar_arrive(bar(kBarPFull + b));
+      tc::mbar_arrive(bar(kBarPFull));
     }
     if (ok) ok = warp_wait(bar(kBarODone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
     if (ok) {
@@ -453,7 +471,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     };
     auto issue_s = [&](int j) {
       const int st = j & 1;
-      const uint32_t d = tmem + static_cast<uint32_t>(st * kKeys);
+      const uint32_t d = tmem + kColS;
       const uint64_t dk = dk0 + st * kStageStep;
 #pragma unroll
       for (int ks = 0; ks < kKSteps; ++ks) {
@@ -473,26 +491,25 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int j = 0; j < ntiles && ok; ++j) {
       const int b = j & 1;
       if (j + 1 < ntiles) {
-        // S_{j+1} overwrites the columns that held P_{j-1}: wait for P_{j-1} V
-        if (j >= 1) ok = tc::mbar_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
-        if (ok) ok = tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+        // S_{j+1} overwrites S_j: wait until the softmax has read it
+        ok = tc::mbar_wait(bar(kBarSFree), j & 1) &&
+             tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
         if (!ok) break;
         tc::tc_fence_after();
         issue_s(j + 1);
         last_bar = bar(kBarSFull + ((j + 1) & 1));
         last_parity = ((j + 1) >> 1) & 1;
       }
-      ok = tc::mbar_wait(bar(kBarPFull + b), (j >> 1) & 1) &&
-           tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
+      ok = tc::mbar_wait(bar(kBarPFull), j & 1) && tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
-      const uint32_t colS = tmem + static_cast<uint32_t>(b * kKeys);
+      const uint32_t colP = tmem + kColP;
       const uint64_t dv = dv0 + b * kStageStep;
 #pragma unroll
       for (int part = 0; part < 2; ++part) {  // weights: head part, then remainder
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks)
-          tc::mma_ts(tmem + kColO, colS + part * 32 + ks * 8, dv + static_cast<uint64_t>(ks * 128),
+          tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + static_cast<uint64_t>(ks * 128),
                      id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
       }
       tc::tc_commit(bar(kBarODone + b));
