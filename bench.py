@@ -441,6 +441,44 @@ def run_copy_blocks(args):
                       "config": {"copies": n, "block_bytes": B * Hkv * d * 2, "dtype": "bf16"}}))
 
 
+def run_cache_write(args):
+    """pa_reshape_and_cache on a full fill (every token of a Llama-3-8B-shaped GQA
+    batch) and on a decode append (one token per sequence): GB/s = 4 T Hkv d e."""
+    import torch
+    import paged_kv_cache_305_gb300 as pa
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    S, Hkv, d, B = 128, 8, 128, 16
+    g = torch.Generator().manual_seed(0)
+    L = torch.randint(1024, 8193, (S,), generator=g)
+    nblk = (L + B - 1) // B
+    pool = int(1.2 * int(nblk.sum()))
+    perm = torch.randperm(pool, generator=g)
+    boff = torch.cumsum(nblk, 0) - nblk
+    seq = torch.repeat_interleave(torch.arange(S), L)
+    t = torch.arange(int(L.sum())) - torch.repeat_interleave(torch.cumsum(L, 0) - L, L)
+    slots = (perm[boff[seq] + t // B] * B + t % B).to(torch.int64).cuda()
+    T = int(L.sum())
+    kc = torch.zeros((pool, B, Hkv, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    k = torch.randn((T, Hkv, d), device="cuda").to(torch.bfloat16)
+    v = torch.randn_like(k)
+    peak, kind = _peaks()
+    res = {}
+    last = (torch.cumsum(L, 0) - 1).cuda()  # each sequence's newest token
+    for name, kk, vv, sl in (("fill", k, v, slots), ("append", k[last], v[last], slots[last])):
+        n = kk.shape[0]
+        ms = _events(lambda: pa.reshape_and_cache(kk, vv, kc, vc, sl), args.steps, max(3, args.warmup))
+        moved = 4 * n * Hkv * d * 2
+        res[name] = {"tokens": n, "ms_per_call": round(ms, 5), "GBps": round(moved / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_hbm_peak": round(moved / (ms * 1e-3) / 1e9 / peak, 4)}
+    print(json.dumps({"op": "cache_write", "metric": "cache write GB/s (read + write of K and V)",
+                      "value": res["fill"]["GBps"], "unit": "GB/s", "peak": peak, "peak_kind": kind,
+                      "fill": res["fill"], "append": res["append"], "steps": args.steps,
+                      "config": {"sequences": S, "num_kv_heads": Hkv, "head_dim": d, "block_size": B,
+                                 "seq_len_range": [1024, 8192], "dtype": "bf16"}}))
+
+
 def run_block_manager(args):
     """Host throughput of the native block manager's append (one token per sequence)."""
     import paged_kv_cache_305_gb300 as pa
@@ -613,14 +651,14 @@ def main():
                     help="fused: pa_decode_append; separate: pa_reshape_and_cache then pa_decode")
     ap.add_argument("--op", default="decode_step",
                     choices=["decode_step", "copy_blocks", "block_manager", "serving_step", "waste",
-                             "prefill"],
+                             "prefill", "cache_write"],
                     help="decode_step is the headline; the others print secondary measurements")
     args = ap.parse_args()
     if args.op != "decode_step":
         if int(os.environ.get("RANK", "0")) == 0:
             {"copy_blocks": run_copy_blocks, "block_manager": run_block_manager,
              "serving_step": run_serving_step, "waste": run_waste,
-             "prefill": run_prefill}[args.op](args)
+             "prefill": run_prefill, "cache_write": run_cache_write}[args.op](args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
