@@ -278,7 +278,11 @@ def run_ours(args, rank, world, local_rank):
     out = torch.empty_like(q)
     ws = pa.alloc_workspace(q, kc, bt, pt)
     stream = torch.cuda.current_stream(dev)
-    fused = args.step == "fused"
+    # pa_decode_append's contract: each sequence's newest token sits in a block
+    # of its own. A workload where some newest tokens sit in shared blocks (a
+    # copy-on-write case the generator marks with slot -1) runs the separate step.
+    fused_ok = bool((case.slot_mapping >= 0).all())
+    fused = args.step == "fused" and fused_ok
 
     def step():
         if fused:  # cache write + attention in one kernel
@@ -374,7 +378,10 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic",
         "config": _config(case, args) | {"partition_tokens": pt or 512,
                                          "step": "pa_decode_append (one kernel)" if fused else
-                                                 "pa_reshape_and_cache + pa_decode"},
+                                                 "pa_reshape_and_cache + pa_decode" +
+                                                 ("" if fused_ok or args.step != "fused" else
+                                                  " (some newest tokens sit in shared blocks: "
+                                                  "the fused write does not apply)")},
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         **({"unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "unique_kv_GBps": round(case.unique_kv_bytes() * K * world / (ms * 1e-3) / 1e9, 2)}

@@ -144,3 +144,44 @@ def test_repeated_calls_are_bit_identical(B):
                    max(qlens), case.scale)
         assert np.array_equal(out.cpu().numpy(), first)
     assert pa.wait_timeout_count(clear=True) == 0
+
+
+def test_full_size_chunked_prefill_sampled():
+    # the configuration bench.py --op prefill times: 16 sequences, 32/8 heads,
+    # d = 128, block size 16, bf16, a 2048-token chunk after 2048 cached tokens;
+    # the oracle computes sampled (sequence, position, kv head) outputs one by one
+    S, Hq, Hkv, d, B, ctx, chunk = 16, 32, 8, 128, 16, 4096, 2048
+    case = W.random_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
+                         len_range=(ctx, ctx), dtype="bf16", seed=0)
+    starts = np.arange(0, (S + 1) * chunk, chunk, dtype=np.int32)
+    q = W.normal_bits((S * chunk, Hq, d), "bf16", 1, 55)
+    dc = DeviceCase(case)
+    qd = dev_bits(q, "bf16")
+    out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    out16 = torch.empty_like(qd)
+    qs = torch.from_numpy(starts).cuda()
+    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale)
+    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale)
+    assert pa.wait_timeout_count(clear=True) == 0
+    got32 = out32.cpu().numpy()
+    got16 = host_bits(out16)
+    del dc, qd, out32, out16
+    torch.cuda.empty_cache()
+    assert np.all(np.isfinite(got32))
+    assert np.array_equal(oracle.round_to_dtype(got32.astype(np.float64), "bf16"), got16)
+    rng = np.random.default_rng(3)
+    G = Hq // Hkv
+    picks = {(0, 0, 0), (S - 1, chunk - 1, Hkv - 1), (5, 63, 2), (5, 64, 2), (7, 127, 3), (7, 128, 3)}
+    while len(picks) < 40:
+        picks.add((int(rng.integers(S)), int(rng.integers(chunk)), int(rng.integers(Hkv))))
+    err = 0.0
+    for s in sorted({p[0] for p in picks}):
+        L = int(case.seq_lens[s])
+        K = oracle.to_float64(oracle.gather_kv(case.key_cache, case.block_tables[s], L, B), "bf16")
+        V = oracle.to_float64(oracle.gather_kv(case.value_cache, case.block_tables[s], L, B), "bf16")
+        for (_, j, h) in [p for p in sorted(picks) if p[0] == s]:
+            pos = L - chunk + j
+            qrow = oracle.to_float64(q[starts[s] + j, h * G:(h + 1) * G], "bf16")
+            ref, _ = oracle.single_query_attention(qrow, K[:pos + 1, h], V[:pos + 1, h], case.scale)
+            err = max(err, float(np.max(np.abs(got32[starts[s] + j, h * G:(h + 1) * G] - ref))))
+    assert err <= ATOL, f"full-size prefill: max |fp32 - oracle| over sampled rows = {err}"

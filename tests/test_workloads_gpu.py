@@ -2,9 +2,11 @@
 
 The oracle computes sampled (sequence, query head) output rows one by one;
 every output row is also checked for properties that hold at any size
-(finite; within the range of the V rows it averages). The step is the one the
-benchmark runs: write each sequence's newest token with pa_reshape_and_cache,
-then pa_decode over the whole sequence.
+(finite; within the range of the V rows it averages). The step: write each
+sequence's newest token with pa_reshape_and_cache, then pa_decode over the
+whole sequence; and, where every newest token has a block of its own, the
+fused pa_decode_append that the benchmark times by default, which must give
+the same bits.
 """
 import numpy as np
 import pytest
@@ -50,6 +52,14 @@ def _run_and_check(case):
     torch.cuda.synchronize()
     got = host_bits(out).copy()
     got32 = dc.decode(out_f32=True).cpu().numpy()
+    if np.all(case.slot_mapping >= 0):
+        # the fused step bench.py times by default: the same bits (its new rows
+        # are the ones the separate write stored, so the caches do not change)
+        fused = torch.empty_like(dc.query)
+        pa.decode_append(fused, dc.query, dc.new_key, dc.new_value, dc.key_cache, dc.value_cache,
+                         dc.block_tables, dc.seq_lens, case.scale, dc.partition_tokens, dc.workspace)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(fused), got)
     # every 16-bit output is the nearest-even rounding of the fp32 result
     assert np.array_equal(oracle.round_to_dtype(got32.astype(np.float64), case.dtype), got)
     # the written rows are where the oracle's write puts them
