@@ -206,22 +206,28 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 
   if (warp < 4) {
     // ---------------- query tile: row r = (position j0 + r / G, head h*G + r % G)
+    // every load issued before any store, so their latencies overlap
     const T* qb = static_cast<const T*>(a.query);
-    for (int i = tid; i < kRows * kChunks; i += 128) {
+    constexpr int kPer = kRows * kChunks / 128;  // 16-byte chunks per thread
+    uint4 qv[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + 128 * k;
       const int r = i / kChunks, c = i % kChunks;
       const int jj = r / G, g = r % G;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      qv[k] = make_uint4(0u, 0u, 0u, 0u);
       if (r < P * G && jj < jn) {
         const size_t row = static_cast<size_t>(q0 + j0 + jj) * a.num_q_heads +
                            static_cast<size_t>(h) * G + g;
-        v = __ldg(reinterpret_cast<const uint4*>(qb + row * D) + c);
-        if (a.scale_log2 < 0.f) {  // q.k * scale == (-q).k * |scale|, exactly
-          v.x ^= 0x80008000u;
-          v.y ^= 0x80008000u;
-          v.z ^= 0x80008000u;
-          v.w ^= 0x80008000u;
-        }
+        qv[k] = __ldg(reinterpret_cast<const uint4*>(qb + row * D) + c);
       }
+    }
+    const uint32_t sign = a.scale_log2 < 0.f ? 0x80008000u : 0u;  // q.k*scale == (-q).k*|scale|
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + 128 * k;
+      const int r = i / kChunks, c = i % kChunks;
+      const uint4 v = make_uint4(qv[k].x ^ sign, qv[k].y ^ sign, qv[k].z ^ sign, qv[k].w ^ sign);
       st_shared_v4(sQ + (c >> 3) * Geo::kQHalf + sw_off(r, c), v);
     }
     tc::fence_async_smem();
@@ -414,16 +420,27 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           const int idi = __shfl_sync(kFull, id, i);
           const int vi = __shfl_sync(kFull, valid, i);
           if ((whole >> i) & 1u) continue;
-          for (int idx = lane; idx < B * kChunks; idx += 32) {
-            const int t = idx / kChunks, c = idx % kChunks;
-            const int row = i * B + t;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (idi >= 0 && t < vi) {
-              const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
-                                 static_cast<size_t>(h) * D + c * 8;
-              v = __ldg(reinterpret_cast<const uint4*>(cache + off));
+          // batches of eight copies per lane: loads first, then stores
+          for (int base = 0; base < B * kChunks; base += 32 * 8) {
+            uint4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + 32 * u + lane;
+              const int t = idx / kChunks, c = idx % kChunks;
+              v[u] = make_uint4(0u, 0u, 0u, 0u);
+              if (idx < B * kChunks && idi >= 0 && t < vi) {
+                const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
+                                   static_cast<size_t>(h) * D + c * 8;
+                v[u] = __ldg(reinterpret_cast<const uint4*>(cache + off));
+              }
             }
-            st_shared_v4(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(row, c), v);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int idx = base + 32 * u + lane;
+              const int t = idx / kChunks, c = idx % kChunks;
+              if (idx < B * kChunks)
+                st_shared_v4(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(i * B + t, c), v[u]);
+            }
           }
         }
         tc::fence_async_smem();

@@ -51,6 +51,8 @@ CASES = [
     ("bf16", 128, 16, 1, 64, (100, 500)),
     ("fp16", 128, 12, 4, 8, (1, 150)),
     ("bf16", 64, 16, 2, 16, (70, 300)),
+    ("fp16", 128, 16, 1, 4, (50, 300)),   # warp-level kernel, 16 query heads per kv head
+    ("bf16", 128, 24, 8, 32, (90, 400)),  # tensor-core kernel, 3 heads per kv head, B = 32
 ]
 
 
