@@ -294,13 +294,23 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:  # the step captured once, replayed every iteration (no host launch cost)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
 
     dec_bytes = case.algorithmic_bytes()
     # the step must also store each new K/V row once (its read is already in
     # dec_bytes as the newest token of its sequence)
     written = 2 * int((case.slot_mapping >= 0).sum()) * case.num_kv_heads * case.head_dim * 2
     step_bytes = dec_bytes + written
-    kern_bytes = step_bytes if fused else dec_bytes
+    # per-iteration events bracket the decode kernel alone, except in graph
+    # mode, where they bracket the replayed step (the write included)
+    kern_bytes = step_bytes if (fused or args.graph) else dec_bytes
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
@@ -316,7 +326,11 @@ def run_ours(args, rank, world, local_rank):
                       int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
         start.record(stream)
         for i in range(K):
-            if fused:
+            if graph is not None:
+                ev[i][0].record(stream)
+                graph.replay()
+                ev[i][1].record(stream)
+            elif fused:
                 ev[i][0].record(stream)
                 pa.decode_append(out, q, nk, nv, kc, vc, bt, sl, case.scale, pt, ws)
                 ev[i][1].record(stream)
@@ -350,6 +364,14 @@ def run_ours(args, rank, world, local_rank):
 
     for _ in range(3):
         e2e_step()
+    if args.graph:  # copies in, the step and the copy out, captured together
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2):
+            e2e_step()
+        e2e_step = g2.replay
+        for _ in range(3):
+            e2e_step()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     Ke = min(K, args.e2e_steps)
@@ -381,7 +403,8 @@ def run_ours(args, rank, world, local_rank):
                                                  "pa_reshape_and_cache + pa_decode" +
                                                  ("" if fused_ok or args.step != "fused" else
                                                   " (some newest tokens sit in shared blocks: "
-                                                  "the fused write does not apply)")},
+                                                  "the fused write does not apply)"),
+                                         "cuda_graph": bool(args.graph)},
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         **({"unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "unique_kv_GBps": round(case.unique_kv_bytes() * K * world / (ms * 1e-3) / 1e9, 2)}
@@ -654,6 +677,8 @@ def main():
     ap.add_argument("--prefill-context", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=2048)
     ap.add_argument("--prefill-block-size", type=int, default=16)
+    ap.add_argument("--graph", action="store_true",
+                    help="capture the step (and the end-to-end step) in CUDA graphs and replay them")
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
                     help="fused: pa_decode_append; separate: pa_reshape_and_cache then pa_decode")
     ap.add_argument("--op", default="decode_step",
