@@ -216,8 +216,9 @@ size_t pa_decode_no_alloc_scratch_bytes(void);
  * upper bound of Q_s (sizes the grid). A Q_s above L or a length above
  * max_blocks_per_seq * block_size is clamped and counted by
  * pa_bad_index_count. Other sizes and errors as for pa_decode.
- * Block sizes 8..64 (with fewer than 2^31 slots) run on the tcgen05 tensor
- * cores with TMA block copies; block sizes 1..4 on the warp-level products.
+ * Runs on the tcgen05 tensor cores (whole blocks of 8..64 tokens copied by
+ * TMA, smaller blocks row by row). num_blocks * block_size must be below 2^31
+ * (PA_ERR_UNSUPPORTED otherwise).
  */
 int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,

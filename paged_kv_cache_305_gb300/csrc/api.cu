@@ -240,6 +240,8 @@ int pa_prefill(void* out, const void* query, const void* key_cache, const void* 
     return fail(PA_ERR_INVALID, "max_blocks_per_seq and num_blocks must be >= 1");
   if (static_cast<long long>(max_blocks_per_seq) * block_size > 0x7fffffffll)
     return fail(PA_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size overflows int");
+  if (!pa::prefill_tc_supported(block_size, static_cast<long long>(num_blocks) * block_size))
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size is 2^31 slots or more");
   if (!isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
   if (max_query_len < 0) return fail(PA_ERR_INVALID, "max_query_len %d < 0", max_query_len);
   if (num_seqs > 65535 || num_kv_heads > 65535)
@@ -274,15 +276,8 @@ int pa_prefill(void* out, const void* query, const void* key_cache, const void* 
   a.bad = bad;
   rc = counter(true, &a.timeouts);
   if (rc != PA_OK) return rc;
-  const bool bf16 = dtype == PA_BFLOAT16;
-  cudaError_t e;
-  if (pa::prefill_tc_supported(block_size, static_cast<long long>(num_blocks) * block_size)) {
-    e = pa::launch_prefill_tc(a, head_dim, bf16, max_query_len, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "paged prefill (tensor-core) launch");
-  } else {
-    e = pa::launch_prefill(a, head_dim, bf16, max_query_len, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
-  }
+  cudaError_t e = pa::launch_prefill_tc(a, head_dim, dtype == PA_BFLOAT16, max_query_len, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
   return PA_OK;
 }
 

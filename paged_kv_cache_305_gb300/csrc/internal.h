@@ -59,9 +59,8 @@ struct PrefillArgs {
   unsigned long long* timeouts;  // bounded waits that gave up (tensor-core kernel)
 };
 
-cudaError_t launch_prefill(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
-                           cudaStream_t stream);
-// Tensor-core (tcgen05 + TMA) prefill: block sizes 8..64, fewer than 2^31 slots.
+// Tensor-core (tcgen05) prefill: block sizes 1..64 (TMA block copies from 8
+// up, 16-byte row copies below), fewer than 2^31 slots.
 bool prefill_tc_supported(int block_size, long long num_slots);
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,
                               cudaStream_t stream);

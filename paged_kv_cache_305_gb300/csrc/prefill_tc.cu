@@ -455,6 +455,67 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tc::tma_load_3d(dst0 + static_cast<uint32_t>(hf * Geo::kTileHalf + i * B * 128), map,
                         full_bar, hf * 64, h, idi * B);
     };
+    if (B < 8) {
+      // Blocks smaller than a swizzle atom: every row by a 16-byte cp.async
+      // (zero fill past L and for rejected ids), two rows per warp
+      // instruction. A tile is announced only once its copies have landed and
+      // been made visible to the tensor cores (fence.proxy.async), one tile
+      // behind the copies in flight.
+      constexpr int kCopies = kKeys * kChunks / 32;  // per lane per tile
+      // lane l holds the block ids of rows l and l + 32 of a tile (-1: none)
+      auto row_ids = [&](int jt, int (&idr)[2]) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int t = jt * kKeys + lane + 32 * u;
+          idr[u] = -1;
+          if (jt < ntiles && t < L) {
+            const int id = __ldg(trow + (t >> shift));
+            if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+              idr[u] = id;
+            else if (!is_v && (t & (B - 1)) == 0)
+              atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
+          }
+        }
+      };
+      auto publish = [&](int jt) {
+        tc::fence_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(bar(full0 + (jt & 1)));
+      };
+      int idn[2];
+      row_ids(0, idn);
+      int j = 0;
+      for (; j < ntiles; ++j) {
+        const int st = j & 1;
+        const int idr[2] = {idn[0], idn[1]};
+        row_ids(j + 1, idn);  // next tile's table entries, ahead of time
+        if (j >= kStages) {
+          ok = warp_wait(bar(empty0 + st), ((j >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+        const uint32_t dst0 = is_v ? sV(st) : sK(st);
+#pragma unroll
+        for (int k = 0; k < kCopies; ++k) {
+          const int idx = 32 * k + lane;
+          const int row = idx / kChunks, c = idx % kChunks;
+          // every lane of this copy reads rows in the same half of the tile
+          const int id = __shfl_sync(kFull, idr[(32 * k / kChunks) >> 5], row & 31);
+          const int t = j * kKeys + row;
+          const bool okr = id >= 0;
+          const size_t off = okr ? ((static_cast<size_t>(id) << shift) + (t & (B - 1))) * slot_stride +
+                                       static_cast<size_t>(h) * D + c * 8
+                                 : 0;
+          cp_async_16(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(row, c), cache + off, okr);
+        }
+        cp_async_commit();
+        if (j >= 1) {
+          cp_async_wait<1>();  // tile j - 1 has landed
+          publish(j - 1);
+        }
+      }
+      cp_async_wait<0>();
+      if (ok && j > 0) publish(j - 1);
+    } else {
     int id_n, valid_n;
     block_of(0, id_n, valid_n);
     int j = 0;
@@ -472,6 +533,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // copies still in flight (only after a wait gave up) must land before exit
     for (int jj = max(0, j - kStages); jj < j; ++jj)
       tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
+    }
   } else if (warp == kMmaWarp && lane == 0) {
     // ---------------- products, one thread; descriptors built once, moved by
     // adding (byte offset >> 4) to the start-address field
@@ -603,7 +665,7 @@ cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stre
 }  // namespace
 
 bool prefill_tc_supported(int block_size, long long num_slots) {
-  return block_size >= 8 && block_size <= 64 && num_slots <= 0x7fffffffll;
+  return block_size >= 1 && block_size <= 64 && num_slots <= 0x7fffffffll;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs& a, int head_dim, bool bf16, int max_query_len,

@@ -51,7 +51,7 @@ CASES = [
     ("bf16", 128, 16, 1, 64, (100, 500)),
     ("fp16", 128, 12, 4, 8, (1, 150)),
     ("bf16", 64, 16, 2, 16, (70, 300)),
-    ("fp16", 128, 16, 1, 4, (50, 300)),   # warp-level kernel, 16 query heads per kv head
+    ("fp16", 128, 16, 1, 4, (50, 300)),   # row copies (B < 8), 16 query heads per kv head
     ("bf16", 128, 24, 8, 32, (90, 400)),  # tensor-core kernel, 3 heads per kv head, B = 32
 ]
 
@@ -99,8 +99,9 @@ def test_unused_slots_are_never_read(B):
     assert np.array_equal(base, nan_out) and np.array_equal(base, inf_out)
 
 
-def test_bad_block_ids_are_counted_not_faulted():
-    case = W.random_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+@pytest.mark.parametrize("B", [16, 2])
+def test_bad_block_ids_are_counted_not_faulted(B):
+    case = W.random_case(num_seqs=3, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=B,
                          len_range=(100, 200), dtype="bf16", seed=41)
     starts = np.array([0, 10, 20, 30], dtype=np.int32)
     dc = DeviceCase(case)
