@@ -131,6 +131,54 @@ def test_cache_write_zero_tokens_is_a_no_op(lib):
     assert _write(lib, T=0, k=None) == 0
 
 
+def _prefill(lib, **kw):
+    a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, S=2, Hq=8, Hkv=2,
+             d=128, B=16, scale=0.1, MB=4, NB=100, mq=64, dtype=1, odt=None)
+    a.update(kw)
+    return lib.pa_prefill(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["sl"], a["qs"], a["S"],
+                          a["Hq"], a["Hkv"], a["d"], a["B"], a["scale"], a["MB"], a["NB"], a["mq"],
+                          a["dtype"], a["dtype"] if a["odt"] is None else a["odt"], None)
+
+
+@pytest.mark.parametrize("kw,code,msg", [
+    (dict(dtype=2), -1, "dtype"),
+    (dict(odt=0), -1, "out_dtype"),
+    (dict(S=-1), -1, "num_seqs"),
+    (dict(Hq=6, Hkv=4), -1, "multiple"),
+    (dict(Hq=34, Hkv=2), -2, "query heads per kv head"),
+    (dict(d=256), -2, "head_dim"),
+    (dict(B=3), -2, "block_size"),
+    (dict(MB=0), -1, "max_blocks_per_seq"),
+    (dict(NB=1 << 27, B=16), -2, "2^31"),
+    (dict(scale=float("nan")), -1, "scale"),
+    (dict(mq=-1), -1, "max_query_len"),
+    (dict(qs=None), -1, "NULL"),
+    (dict(out=FAKE + 8), -1, "aligned"),
+    (dict(qs=FAKE + 2), -1, "aligned"),
+])
+def test_prefill_rejects_bad_arguments(lib, kw, code, msg):
+    assert _prefill(lib, **kw) == code
+    assert msg in pa.last_error()
+
+
+def test_prefill_empty_calls_are_no_ops(lib):
+    assert _prefill(lib, S=0, out=None) == 0
+    assert _prefill(lib, mq=0, out=None) == 0
+
+
+def test_copy_blocks_rejects_bad_arguments(lib):
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, -1, 2, 128, 16, 10, 1, None) == -1
+    assert lib.pa_copy_blocks(FAKE, FAKE, FAKE, FAKE, 1, 2, 80, 16, 10, 1, None) == -2
+    assert lib.pa_copy_blocks(FAKE, FAKE, None, FAKE, 1, 2, 128, 16, 10, 1, None) == -1
+    assert "NULL" in pa.last_error()
+    assert lib.pa_copy_blocks(None, None, None, None, 0, 2, 128, 16, 10, 1, None) == 0
+
+
+def test_wait_timeout_count_rejects_null(lib):
+    assert lib.pa_wait_timeout_count(None, 0) == -1
+    assert "NULL" in pa.last_error()
+
+
 def test_bad_index_count_rejects_null(lib):
     assert lib.pa_bad_index_count(None, 0) == -1
     assert "NULL" in pa.last_error()
