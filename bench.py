@@ -466,7 +466,9 @@ def run_ours(args, rank, world, local_rank):
                      "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
                      "algorithmic_bytes": kern_bytes,
                      "mean_launch_us": round(dec_mean_ms * 1e3, 2),
-                     "median_launch_us": round(statistics.median(dec_ms) * 1e3, 2)},
+                     "median_launch_us": round(statistics.median(dec_ms) * 1e3, 2),
+                     "min_launch_us": round(min(dec_ms) * 1e3, 2),
+                     "p90_launch_us": round(sorted(dec_ms)[int(0.9 * (len(dec_ms) - 1))] * 1e3, 2)},
         "e2e": {"value": round(step_bytes * Ke * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke},
         "gpu_launches": K if fused else 2 * K,
