@@ -1,9 +1,9 @@
-// Paged causal prefill on the tcgen05 tensor cores (block sizes 8..64).
+// Paged causal prefill on the tcgen05 tensor cores (block sizes 1..64).
 //
-// Same operation as the other prefill kernel ("PagedAttention" glossary, How
-// It Works: the blockwise formula with query index i, read token by token):
-// query j of sequence s's Q-token chunk sits at position L - Q + j and
-// attends to tokens 0 .. L - Q + j of the paged cache.
+// The operation ("PagedAttention" glossary, How It Works: the blockwise
+// formula with query index i, read token by token): query j of sequence s's
+// Q-token chunk sits at position L - Q + j and attends to tokens
+// 0 .. L - Q + j of the paged cache.
 //
 // One CTA per (query tile, kv head, sequence). A query tile is 128 rows =
 // 128 / G positions x the G heads of the kv head (the product's M), so each
@@ -18,10 +18,11 @@
 //              max has grown by more than 2^8 since the last rescale; finally
 //              divides by the sum and stores the row.
 //   warps 4, 5 producers of the K and the V tiles (each on its own, so K
-//              runs ahead of V): whole blocks by TMA (one box per block and
-//              64-element half of the head dim, straight from the block
-//              table), partial / out-of-range blocks by plain loads with zero
-//              fill; two stages, a K stage reused as soon as its S is done.
+//              runs ahead of V): whole blocks of 8+ tokens by TMA (one box
+//              per block and 64-element half of the head dim, straight from
+//              the block table), partial / out-of-range blocks by plain loads
+//              with zero fill; blocks under 8 tokens row by row with 16-byte
+//              cp.async; two stages, a K stage reused as soon as its S is done.
 //   warp 6     one thread issues the products: S_{j+1} = Q K_{j+1}^T (smem x
 //              smem, M=128, N=64) as soon as the softmax has read S_j, and
 //              O += P_j V_j (weights from tensor memory, V from smem read
