@@ -19,8 +19,8 @@
 //              divides by the sum and stores the row.
 //   warps 4, 5 producers of the K and the V tiles (each on its own, so K
 //              runs ahead of V): whole blocks of 8+ tokens by TMA (one box
-//              per block and 64-element half of the head dim, straight from
-//              the block table), partial / out-of-range blocks by plain loads
+//              per block, the whole head dim, straight from the block
+//              table), partial / out-of-range blocks by plain loads
 //              with zero fill; blocks under 8 tokens row by row with 16-byte
 //              cp.async; two stages, a K stage reused as soon as its S is done.
 //   warp 6     one thread issues the products: S_{j+1} = Q K_{j+1}^T (smem x
@@ -64,8 +64,12 @@ struct TcGeo {
   static constexpr int kHalves = D / 64;           // 128-byte row slices of the head dim
   static constexpr int kQHalf = kRows * 128;        // one slice of the query tile
   static constexpr int kQBytes = kHalves * kQHalf;
-  static constexpr int kTileHalf = kKeys * 128;     // one slice of a K or V tile
-  static constexpr int kTileBytes = kHalves * kTileHalf;
+  // K and V tiles: 8-token groups of the whole head dim (kGroupBytes), in
+  // a group the 64-element slices one after the other, each 8 rows of 128
+  // bytes; one group of one block is exactly what a cache block holds for
+  // 8 of its tokens, so a whole block lands with one copy
+  static constexpr int kGroupBytes = kHalves * 1024;
+  static constexpr int kTileBytes = kKeys * D * 2;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
   static constexpr int kBarOff = kQBytes + kStages * kStageBytes;
   // barriers + alignment slack; at least 80 KB so that no more than two CTAs
@@ -96,6 +100,13 @@ enum : int {
 // slice (the slice itself, chunk >> 3, is added by the caller).
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// Offset of 16-byte chunk c of token t inside a K or V tile.
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int t, int c) {
+  return static_cast<uint32_t>((t >> 3) * TcGeo<D>::kGroupBytes + (c >> 3) * 1024) +
+         sw_off(t & 7, c);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -389,8 +400,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     const int full0 = is_v ? kBarVFull : kBarKFull;
     const int empty0 = is_v ? kBarODone : kBarSFull;  // stage free once S_j / P_j V is done
-    if (lane == 0) tc::prefetch_tensormap(map);
     const int B = 1 << shift;
+    if (lane == 0 && B >= 8) tc::prefetch_tensormap(map);  // no map below 8
     const int nb = kKeys >> shift;  // blocks per tile (1..8)
     const int32_t* trow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
     const size_t slot_stride = static_cast<size_t>(a.num_kv_heads) * D;
@@ -421,26 +432,25 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           const int idi = __shfl_sync(kFull, id, i);
           const int vi = __shfl_sync(kFull, valid, i);
           if ((whole >> i) & 1u) continue;
+          // lane: chunk lane % kChunks of rows lane / kChunks + kLaneRows * u;
           // batches of eight copies per lane: loads first, then stores
-          for (int base = 0; base < B * kChunks; base += 32 * 8) {
+          constexpr int kLaneRows = 32 / kChunks;
+          const int c = lane % kChunks;
+          const T* src = cache + (static_cast<size_t>(max(idi, 0)) << shift) * slot_stride +
+                         static_cast<size_t>(h) * D + c * 8;
+          for (int t0 = lane / kChunks; t0 < B; t0 += 8 * kLaneRows) {
             uint4 v[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const int idx = base + 32 * u + lane;
-              const int t = idx / kChunks, c = idx % kChunks;
+              const int t = t0 + kLaneRows * u;
               v[u] = make_uint4(0u, 0u, 0u, 0u);
-              if (idx < B * kChunks && idi >= 0 && t < vi) {
-                const size_t off = ((static_cast<size_t>(idi) << shift) + t) * slot_stride +
-                                   static_cast<size_t>(h) * D + c * 8;
-                v[u] = __ldg(reinterpret_cast<const uint4*>(cache + off));
-              }
+              if (t < vi && idi >= 0)
+                v[u] = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(t) * slot_stride));
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
-              const int idx = base + 32 * u + lane;
-              const int t = idx / kChunks, c = idx % kChunks;
-              if (idx < B * kChunks)
-                st_shared_v4(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(i * B + t, c), v[u]);
+              const int t = t0 + kLaneRows * u;
+              if (t < B) st_shared_v4(dst0 + kv_off<D>(i * B + t, c), v[u]);
             }
           }
         }
@@ -450,11 +460,9 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       if (lane == 0)
         tc::mbar_arrive_expect_tx(full_bar, static_cast<uint32_t>(__popc(whole)) * B * D * 2);
       __syncwarp();
-      const int i = lane / Geo::kHalves, hf = lane % Geo::kHalves;
-      const int idi = __shfl_sync(kFull, id, i & 31);
-      if (i < nb && ((whole >> i) & 1u))
-        tc::tma_load_3d(dst0 + static_cast<uint32_t>(hf * Geo::kTileHalf + i * B * 128), map,
-                        full_bar, hf * 64, h, idi * B);
+      if ((whole >> lane) & 1u)  // lane i: block i, all B / 8 groups, whole head dim
+        tc::tma_load_5d(dst0 + static_cast<uint32_t>(lane * B * D * 2), map, full_bar, 0, 0, 0,
+                        id << (shift - 3), h);
     };
     if (B < 8) {
       // Blocks smaller than a swizzle atom: every row by a 16-byte cp.async
@@ -506,7 +514,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           const size_t off = okr ? ((static_cast<size_t>(id) << shift) + (t & (B - 1))) * slot_stride +
                                        static_cast<size_t>(h) * D + c * 8
                                  : 0;
-          cp_async_16(dst0 + (c >> 3) * Geo::kTileHalf + sw_off(row, c), cache + off, okr);
+          cp_async_16(dst0 + kv_off<D>(row, c), cache + off, okr);
         }
         cp_async_commit();
         if (j >= 1) {
@@ -541,13 +549,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
     const uint32_t id_o = tc::idesc_f16(kRows, D, Ty::kIsBf16, true);
     const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
-    const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, 1024);
-    // V read MN-major: 8-token groups 1024 bytes apart (SBO), the two
-    // 64-element slices of the head dim kTileHalf apart (LBO)
-    const uint64_t dv0 = tc::sdesc_sw128(sV(0), Geo::kHalves > 1 ? Geo::kTileHalf : 16, 1024);
+    // K read K-major: 8-token groups kGroupBytes apart (SBO)
+    const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, Geo::kGroupBytes);
+    // V read MN-major: 8-token groups kGroupBytes apart (SBO), the two
+    // 64-element slices of the head dim 1024 bytes apart (LBO)
+    const uint64_t dv0 = tc::sdesc_sw128(sV(0), Geo::kHalves > 1 ? 1024 : 16, Geo::kGroupBytes);
     constexpr uint64_t kStageStep = Geo::kStageBytes >> 4;
+    constexpr uint64_t kVStep = (2 * Geo::kGroupBytes) >> 4;  // 16 tokens
     auto kstep = [](int ks) {  // K-major: slice ks / 4, 32 bytes per 16 elements
-      return static_cast<uint64_t>(((ks >> 2) * Geo::kTileHalf + (ks & 3) * 32) >> 4);
+      return static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
     };
     auto issue_s = [&](int j) {
       const int st = j & 1;
@@ -589,7 +599,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       for (int part = 0; part < 2; ++part) {  // weights: head part, then remainder
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks)
-          tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + static_cast<uint64_t>(ks * 128),
+          tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
                      id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
       }
       tc::tc_commit(bar(kBarODone + b));
@@ -625,19 +635,28 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return f;
 }
 
-// One cache viewed as [num_blocks * B slots, Hkv, d]; a box is one block of
-// one kv head, 64 elements of the head dim wide, 128-byte swizzle.
-bool encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, int num_slots, int hkv, int d,
-                      int block_size) {
+// One cache [num_blocks * B slots, Hkv, d] viewed, innermost first, as
+// (64 elements of a head-dim slice, 8 slots of a group, d / 64 slices,
+// slot groups, kv head); a box is one block of one kv head: (64, 8, d / 64,
+// B / 8, 1), which lands in the tile layout of the products (8-token groups
+// of the whole head dim, 128-byte swizzle). Only for B >= 8 (a multiple of 8
+// slots); smaller blocks are copied row by row and get no map.
+bool encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, long long num_slots, int hkv,
+                      int d, int block_size) {
+  if (block_size < 8) {
+    *map = CUtensorMap{};
+    return true;
+  }
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(hkv),
-                              static_cast<cuuint64_t>(num_slots)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                 static_cast<cuuint64_t>(hkv) * d * 2};
-  const cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(block_size)};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+  const cuuint64_t row = static_cast<cuuint64_t>(hkv) * d * 2;  // bytes per slot
+  const cuuint64_t dims[5] = {64, 8, static_cast<cuuint64_t>(d / 64),
+                              static_cast<cuuint64_t>(num_slots / 8), static_cast<cuuint64_t>(hkv)};
+  const cuuint64_t strides[4] = {row, 128, 8 * row, static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[5] = {64, 8, static_cast<cuuint32_t>(d / 64),
+                             static_cast<cuuint32_t>(block_size / 8), 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5,
              const_cast<void*>(cache), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -650,10 +669,10 @@ cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stre
   if (tiles < 1) return cudaSuccess;
   const long long slots = static_cast<long long>(a.num_blocks) << a.block_shift;
   CUtensorMap km, vm;
-  if (!encode_cache_map(&km, a.key_cache, Ty::kIsBf16, static_cast<int>(slots), a.num_kv_heads, D,
+  if (!encode_cache_map(&km, a.key_cache, Ty::kIsBf16, slots, a.num_kv_heads, D,
                         1 << a.block_shift) ||
-      !encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, static_cast<int>(slots), a.num_kv_heads,
-                        D, 1 << a.block_shift))
+      !encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, slots, a.num_kv_heads, D,
+                        1 << a.block_shift))
     return cudaErrorInvalidValue;
   auto kern = paged_prefill_tc_kernel<Ty, D>;
   cudaError_t e =
