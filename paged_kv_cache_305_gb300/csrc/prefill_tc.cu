@@ -12,8 +12,10 @@
 //   warps 0-3  one thread per query row: loads the query tile, then for every
 //              key tile reads its row of S = q K^T from tensor memory (and at
 //              once frees the S columns for the next tile's product), applies
-//              the causal limit, keeps the running max / sum (base 2), writes
-//              the weights into tensor memory as a 16-bit head plus the 16-bit
+//              the causal limit (only in warps holding a diagonal tile: a
+//              warp-uniform branch, so other tiles carry no per-element
+//              selects), keeps the running max / sum (base 2), writes the
+//              weights into tensor memory as a 16-bit head plus the 16-bit
 //              rounding of the remainder, and rescales its output row when the
 //              max has grown by more than 2^8 since the last rescale; finally
 //              divides by the sum and stores the row.
@@ -37,6 +39,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -115,7 +118,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-// Packed pairs of fp32 (one 64-bit register) and the paired fp32 operations
+// Packed pairs of fp32 (one 64-bit register) and the paired fp32 multiply-add
 // of sm_100-family cores, plus the three-input max: fewer instructions in the
 // per-row softmax.
 __device__ __forceinline__ uint64_t f2(float a, float b) {
@@ -131,16 +134,6 @@ __device__ __forceinline__ float2 f2_split(uint64_t r) {
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
-__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ float max3(float a, float b, float c) {
@@ -278,55 +271,72 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       // S_j is in registers: S_{j+1} may now be written into the same columns
       tc::tc_fence_before();
       tc::mbar_arrive(bar(kBarSFree));
-      // tokens kb + c with c > lim are past this row's causal limit
+      // tokens kb + c with c > lim are past this row's causal limit; a warp
+      // with any such row takes the masked path, the others carry no
+      // per-element selects (warp-uniform branch)
       const int lim = qp - j * kKeys;
-      const bool diag = lim < kKeys - 1;
-      if (diag) {
-#pragma unroll
-        for (int c = 0; c < kKeys; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
-      }
-      // row max of the raw scores: four chains of three-input maxima
-      float mx4[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float* v = sv + 16 * q4;
-        float mq = max3(v[0], v[1], v[2]);
-#pragma unroll
-        for (int c = 3; c < 15; c += 2) mq = max3(mq, v[c], v[c + 1]);
-        mx4[q4] = fmaxf(mq, v[15]);
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
-      const bool rescale = __any_sync(kFull, mn > m + kRescaleLog2);
+      const bool diag = __any_sync(kFull, lim < kKeys - 1);
+      bool rescale = false;
       float alpha = 1.f;
-      if (rescale) {
-        alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
-        l *= alpha;
-        m = mn;
-      }
-      // weights 2^(s*sl2 - m) as a 16-bit head and the 16-bit rounding of the
-      // remainder, held in registers; paired fp32 arithmetic, four partial sums
-      const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
-      uint64_t rs2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t ph[32], pl[32];
+      auto weights = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
+        if constexpr (kMasked) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int c = 2 * i;
-        const float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
-        float p0 = ex2(arg.x), p1 = ex2(arg.y);
-        if (diag) {  // exact zeros past the limit (also for a zero scale)
-          p0 = c > lim ? 0.f : p0;
-          p1 = c + 1 > lim ? 0.f : p1;
+          for (int c = 0; c < kKeys; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
         }
-        const uint64_t pp = f2(p0, p1);
-        rs2[i & 3] = f2_add(rs2[i & 3], pp);
-        ph[i] = Ty::pack(p0, p1);
-        const float2 d = Ty::unpack(ph[i]);
-        const float2 r = f2_split(f2_sub(pp, f2(d.x, d.y)));
-        pl[i] = Ty::pack(r.x, r.y);
-      }
-      const float2 ra = f2_split(f2_add(rs2[0], rs2[1])), rb = f2_split(f2_add(rs2[2], rs2[3]));
-      l += (ra.x + ra.y) + (rb.x + rb.y);
+        // row max of the raw scores: four chains of three-input maxima
+        float mx4[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* v = sv + 16 * q4;
+          float mq = max3(v[0], v[1], v[2]);
+#pragma unroll
+          for (int c = 3; c < 15; c += 2) mq = max3(mq, v[c], v[c + 1]);
+          mx4[q4] = fmaxf(mq, v[15]);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
+        rescale = __any_sync(kFull, mn > m + kRescaleLog2);
+        if (rescale) {
+          alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
+          l *= alpha;
+          m = mn;
+        }
+        // weights 2^(s*sl2 - m), held in registers as a 16-bit head and the
+        // 16-bit rounding of the remainder (bf16: the head is the upper half
+        // of the fp32 weight, taken by byte selection; fp16: rounded);
+        // the exponent arguments by paired fp32 multiply-adds
+        const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(-m, -m);
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 2 * i;
+          float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
+          if constexpr (kMasked) {  // exact zeros past the limit (also for a zero scale)
+            arg.x = c > lim ? -INFINITY : arg.x;
+            arg.y = c + 1 > lim ? -INFINITY : arg.y;
+          }
+          const float p0 = ex2(arg.x), p1 = ex2(arg.y);
+          rs[i & 3] += p0;
+          rs[i & 3] += p1;
+          if constexpr (Ty::kIsBf16) {
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            ph[i] = __byte_perm(b0, b1, 0x7632);
+            pl[i] = Ty::pack(p0 - __uint_as_float(b0 & 0xffff0000u),
+                             p1 - __uint_as_float(b1 & 0xffff0000u));
+          } else {
+            ph[i] = Ty::pack(p0, p1);
+            const float2 d = Ty::unpack(ph[i]);
+            pl[i] = Ty::pack(p0 - d.x, p1 - d.y);
+          }
+        }
+        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      };
+      if (diag)
+        weights(std::true_type{});
+      else
+        weights(std::false_type{});
       if (j > 0) {
         // P_{j-1} V must be done before P_j overwrites its columns and O is rescaled
         ok = warp_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
