@@ -84,6 +84,18 @@ def test_long_prompt_many_tiles():
     _run(case, [1500, 1000], 5)
 
 
+@pytest.mark.parametrize("B", [16, 4])
+def test_many_sequences_ragged_chunks(B):
+    # thousands of (query tile, kv head, sequence) CTAs, several waves per SM,
+    # chunks of every length (some empty, some whole prompts); B = 4 takes
+    # the row-copy producers
+    case = W.random_case(num_seqs=48, num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=B,
+                         len_range=(1, 400), dtype="bf16", seed=90 + B)
+    qlens = [int(x) if i % 3 else int(x) // 2 for i, x in enumerate(case.seq_lens)]
+    qlens[5] = 0
+    _run(case, qlens, 13)
+
+
 @pytest.mark.parametrize("B", [8, 16, 64, 2])
 def test_unused_slots_are_never_read(B):
     # tail slots of each last block and blocks outside the tables hold NaN / Inf:
