@@ -190,10 +190,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   auto sK = [&](int st) { return sKV + static_cast<uint32_t>(st * Geo::kStageBytes); };
   auto sV = [&](int st) { return sK(st) + static_cast<uint32_t>(Geo::kTileBytes); };
 
+  // blocks under 8 tokens arrive row by row: every producer lane signals its
+  // own copies' completion on the tile's barrier
+  const bool row_copies = shift < 3;
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(bar(kBarKFull + i), 1);
-      tc::mbar_init(bar(kBarVFull + i), 1);
+      tc::mbar_init(bar(kBarKFull + i), row_copies ? 32 : 1);
+      tc::mbar_init(bar(kBarVFull + i), row_copies ? 32 : 1);
       tc::mbar_init(bar(kBarSFull + i), 1);
       tc::mbar_init(bar(kBarODone + i), 1);
     }
@@ -477,9 +480,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     if (B < 8) {
       // Blocks smaller than a swizzle atom: every row by a 16-byte cp.async
       // (zero fill past L and for rejected ids), two rows per warp
-      // instruction. A tile is announced only once its copies have landed and
-      // been made visible to the tensor cores (fence.proxy.async), one tile
-      // behind the copies in flight.
+      // instruction. Each lane then arrives on the tile's barrier when its
+      // copies have landed (cp.async.mbarrier.arrive.noinc, 32 arrivals per
+      // tile); the product thread makes them visible to the tensor cores
+      // (fence.proxy.async) after its wait.
       constexpr int kCopies = kKeys * kChunks / 32;  // per lane per tile
       // lane l holds the block ids of rows l and l + 32 of a tile (-1: none)
       auto row_ids = [&](int jt, int (&idr)[2]) {
@@ -495,11 +499,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
               atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
           }
         }
-      };
-      auto publish = [&](int jt) {
-        tc::fence_async_smem();
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(full0 + (jt & 1)));
       };
       int idn[2];
       row_ids(0, idn);
@@ -526,14 +525,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                                  : 0;
           cp_async_16(dst0 + kv_off<D>(row, c), cache + off, okr);
         }
-        cp_async_commit();
-        if (j >= 1) {
-          cp_async_wait<1>();  // tile j - 1 has landed
-          publish(j - 1);
-        }
+        tc::cp_async_mbar_arrive_noinc(bar(full0 + st));
       }
-      cp_async_wait<0>();
-      if (ok && j > 0) publish(j - 1);
+      // copies still in flight (only after a wait gave up) land before exit
+      for (int jj = max(0, j - kStages); jj < j; ++jj)
+        tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
     } else {
     int id_n, valid_n;
     block_of(0, id_n, valid_n);
@@ -584,6 +580,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     ok = tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
     if (ok) {
       tc::tc_fence_after();
+      if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products
       issue_s(0);
       last_bar = bar(kBarSFull);
       last_parity = 0;
@@ -596,6 +593,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
              tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
         if (!ok) break;
         tc::tc_fence_after();
+        if (row_copies) tc::fence_async_smem();
         issue_s(j + 1);
         last_bar = bar(kBarSFull + ((j + 1) & 1));
         last_parity = ((j + 1) >> 1) & 1;
@@ -603,6 +601,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       ok = tc::mbar_wait(bar(kBarPFull), j & 1) && tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
       if (!ok) break;
       tc::tc_fence_after();
+      if (row_copies) tc::fence_async_smem();
       const uint32_t colP = tmem + kColP;
       const uint64_t dv = dv0 + b * kStageStep;
 #pragma unroll

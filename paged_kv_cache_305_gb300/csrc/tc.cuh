@@ -58,6 +58,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// One arrival on bar once every cp.async this thread issued so far has
+// landed (the barrier's expected count is not raised: it must be initialised
+// with one arrival per thread that signals this way).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (TMA,
 // tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_async_smem() {
