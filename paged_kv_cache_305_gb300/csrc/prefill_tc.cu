@@ -486,27 +486,34 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       // (fence.proxy.async) after its wait.
       constexpr int kCopies = kKeys * kChunks / 32;  // per lane per tile
       // lane l holds the block ids of rows l and l + 32 of a tile (-1: none)
-      auto row_ids = [&](int jt, int (&idr)[2]) {
+      // lane l holds the cache slots of rows l and l + 32 of a tile (-1:
+      // past L or a rejected block id); slots stay below 2^31
+      auto row_slots = [&](int jt, int (&sr)[2]) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int t = jt * kKeys + lane + 32 * u;
-          idr[u] = -1;
+          sr[u] = -1;
           if (jt < ntiles && t < L) {
             const int id = __ldg(trow + (t >> shift));
             if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
-              idr[u] = id;
+              sr[u] = (id << shift) + (t & (B - 1));
             else if (!is_v && (t & (B - 1)) == 0)
               atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
           }
         }
       };
-      int idn[2];
-      row_ids(0, idn);
+      // this lane's 16-byte chunk of a row: c = lane % kChunks, rows
+      // kLaneRows * k + lane / kChunks
+      constexpr int kLaneRows = 32 / kChunks;
+      const int c = lane % kChunks, r0 = lane / kChunks;
+      const T* cbase = cache + static_cast<size_t>(h) * D + c * 8;
+      int sn[2];
+      row_slots(0, sn);
       int j = 0;
       for (; j < ntiles; ++j) {
         const int st = j & 1;
-        const int idr[2] = {idn[0], idn[1]};
-        row_ids(j + 1, idn);  // next tile's table entries, ahead of time
+        const int sr[2] = {sn[0], sn[1]};
+        row_slots(j + 1, sn);  // next tile's table entries, ahead of time
         if (j >= kStages) {
           ok = warp_wait(bar(empty0 + st), ((j >> 1) - 1) & 1);
           if (!ok) break;
@@ -514,16 +521,12 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const uint32_t dst0 = is_v ? sV(st) : sK(st);
 #pragma unroll
         for (int k = 0; k < kCopies; ++k) {
-          const int idx = 32 * k + lane;
-          const int row = idx / kChunks, c = idx % kChunks;
+          const int row = kLaneRows * k + r0;
           // every lane of this copy reads rows in the same half of the tile
-          const int id = __shfl_sync(kFull, idr[(32 * k / kChunks) >> 5], row & 31);
-          const int t = j * kKeys + row;
-          const bool okr = id >= 0;
-          const size_t off = okr ? ((static_cast<size_t>(id) << shift) + (t & (B - 1))) * slot_stride +
-                                       static_cast<size_t>(h) * D + c * 8
-                                 : 0;
-          cp_async_16(dst0 + kv_off<D>(row, c), cache + off, okr);
+          const int slot = __shfl_sync(kFull, sr[(kLaneRows * k) >> 5], row & 31);
+          const bool okr = slot >= 0;
+          cp_async_16(dst0 + kv_off<D>(row, c),
+                      cbase + static_cast<size_t>(okr ? slot : 0) * slot_stride, okr);
         }
         tc::cp_async_mbar_arrive_noinc(bar(full0 + st));
       }
