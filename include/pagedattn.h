@@ -128,7 +128,9 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  * Sizes: num_seqs >= 0 (0 is a no-op) and <= 65535, num_kv_heads in
  * [1, 65535], num_q_heads a multiple of num_kv_heads with at most 16 query
  * heads per kv head, head_dim in {64, 128}, block_size a power of two in
- * [1, 64], max_blocks_per_seq >= 1, num_blocks >= 1, scale finite.
+ * [1, 64], max_blocks_per_seq >= 1, num_blocks >= 1 with num_blocks *
+ * block_size below 2^32 - 1 slots (PA_ERR_UNSUPPORTED otherwise; such a pool
+ * would not fit in one GPU's memory), scale finite.
  * A seq_len above max_blocks_per_seq * block_size is clamped to it, and a
  * block id outside [0, num_blocks) reads as zeros; both are counted by
  * pa_bad_index_count and never fault.

@@ -330,6 +330,9 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
     return fail(PA_ERR_UNSUPPORTED, "block_size %d (supported: powers of two up to 64)", block_size);
   if (max_blocks_per_seq < 1) return fail(PA_ERR_INVALID, "max_blocks_per_seq %d < 1", max_blocks_per_seq);
   if (num_blocks < 1) return fail(PA_ERR_INVALID, "num_blocks %d < 1", num_blocks);
+  // cache slots travel as 32-bit values in the kernel (all ones = none)
+  if ((static_cast<long long>(num_blocks) << shift) > 0xfffffffeLL)
+    return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size is 2^32 - 1 slots or more");
   if (!isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
   int pt = 0;
   rc = resolve_partition(partition_tokens, block_size, &pt);

@@ -325,18 +325,26 @@ paged_decode_kernel(const DecodeArgs a) {
         j = ws;
       }
     };
-    // table id of row (lane & 15) of a tile (validated when the copy is issued)
-    auto load_id = [&](int sg, int j) -> int {
-      if (sg >= nseg) return 0;
+    // cache slot of row (lane & 15) of a tile: kNoSlot past the segment's
+    // end and for a rejected block id (counted once per row, its rows read
+    // as zero); the copies then need one shuffle and one multiply each
+    constexpr uint32_t kNoSlot = 0xffffffffu;
+    auto load_id = [&](int sg, int j) -> uint32_t {
+      if (sg >= nseg) return kNoSlot;
       const Seg& g = sSeg[sg];
       const int t = g.t0 + j * kTileTokens + (lane & 15);
-      if (t >= g.t1) return 0;
-      return __ldg(a.block_tables + static_cast<size_t>(g.s) * a.max_blocks_per_seq + (t >> shift));
+      if (t >= g.t1) return kNoSlot;
+      const int phys = __ldg(a.block_tables + static_cast<size_t>(g.s) * a.max_blocks_per_seq + (t >> shift));
+      if (static_cast<unsigned>(phys) >= static_cast<unsigned>(a.num_blocks)) {
+        if (lane < 16) atomicAdd(a.bad, 1ull);
+        return kNoSlot;
+      }
+      return (static_cast<uint32_t>(phys) << shift) + static_cast<uint32_t>(t & bmask);
     };
     int id_sg = 0, id_j = ws - Wh;
     advance(id_sg, id_j);
     int is_sg = id_sg, is_j = id_j;
-    int idq[kIdDepth];
+    uint32_t idq[kIdDepth];
 #pragma unroll
     for (int k = 0; k < kIdDepth; ++k) {
       idq[k] = load_id(id_sg, id_j);
@@ -360,12 +368,9 @@ paged_decode_kernel(const DecodeArgs a) {
         const int fresh_r = fresh_tile ? g.L - 1 - tb : -1;
         auto copy = [&](int i, bool check_fresh) {
           const int r = cr + i * kRowsPerCopy;
-          const int phys = __shfl_sync(kFull, idq[0], r);
-          const int t = tb + r;
-          const bool in = t < g.t1;
-          const bool ok = in && static_cast<unsigned>(phys) < static_cast<unsigned>(a.num_blocks);
-          if (in && !ok && cc == 0) atomicAdd(a.bad, 1ull);  // rejected id: its rows read as zero
-          const size_t slot = ok ? (static_cast<size_t>(phys) << shift) + (t & bmask) : 0;
+          const uint32_t sl = __shfl_sync(kFull, idq[0], r);
+          const bool ok = sl != kNoSlot;
+          const size_t slot = ok ? sl : 0u;
           const uint32_t off = r * kRowBytes + swz(r, cc);
           if (check_fresh && r == fresh_r) {
             const size_t nrow = (static_cast<size_t>(g.s) * Hkv + h) * D + cc * 8;
