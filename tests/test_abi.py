@@ -84,6 +84,7 @@ def _decode(lib, **kw):
     (dict(B=128), -2, "block_size"),
     (dict(MB=0), -1, "max_blocks_per_seq"),
     (dict(NB=0), -1, "num_blocks"),
+    (dict(NB=1 << 27, B=64), -2, "slots"),           # 2^33 slots: above the 32-bit slot range
     (dict(scale=float("inf")), -1, "scale"),
     (dict(pt=24), -1, "partition_tokens"),
     (dict(pt=16, B=32), -1, "partition_tokens"),
