@@ -682,9 +682,10 @@ def run_prefill(args):
     pbuild.build()
     S, Hq, Hkv, d, B = 16, 32, 8, 128, args.prefill_block_size
     ctx, chunk = args.prefill_context, args.prefill_chunk
+    tname = args.prefill_dtype
     case = W.random_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
-                         len_range=(ctx, ctx), dtype="bf16", seed=0)
-    dt = torch.bfloat16
+                         len_range=(ctx, ctx), dtype=tname, seed=0)
+    dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[tname]
     up = lambda b: torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).cuda().view(dt)
     kc, vc = up(case.key_cache), up(case.value_cache)
     bt = torch.from_numpy(case.block_tables).cuda()
@@ -698,15 +699,16 @@ def run_prefill(args):
     flops = 4.0 * d * Hq * pairs
     tf = flops / (ms * 1e-3) / 1e12
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    # fp16 and bf16 products run at the same dense tensor rate
     peak = float(json.load(open(p))["bf16_tflops"]) if os.path.exists(p) else 1900.0
     print(json.dumps({"op": "prefill", "metric": "paged causal prefill TFLOP/s (algorithmic)",
                       "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
                       "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
-                                   "peak_kind": "measured bf16_tflops (cuBLAS, burst)",
+                                   "peak_kind": "measured bf16_tflops (cuBLAS, burst; fp16 has the same nominal rate)",
                                    "frac": round(tf / peak, 4)},
                       "tokens_per_s": round(S * chunk / (ms * 1e-3), 1), "steps": args.steps,
                       "config": {"sequences": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
-                                 "block_size": B, "context": ctx, "chunk": chunk, "dtype": "bf16"}}))
+                                 "block_size": B, "context": ctx, "chunk": chunk, "dtype": tname}}))
 
 
 def main():
@@ -728,6 +730,7 @@ def main():
     ap.add_argument("--prefill-context", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=2048)
     ap.add_argument("--prefill-block-size", type=int, default=16)
+    ap.add_argument("--prefill-dtype", default="bf16", choices=["bf16", "fp16"])
     ap.add_argument("--graph", action="store_true",
                     help="capture the step (and the end-to-end step) in CUDA graphs and replay them")
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
