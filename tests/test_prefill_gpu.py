@@ -53,6 +53,8 @@ CASES = [
     ("bf16", 64, 16, 2, 16, (70, 300)),
     ("fp16", 128, 16, 1, 4, (50, 300)),   # row copies (B < 8), 16 query heads per kv head
     ("bf16", 128, 24, 8, 32, (90, 400)),  # tensor-core kernel, 3 heads per kv head, B = 32
+    ("bf16", 64, 8, 8, 64, (60, 600)),    # d = 64 (one head-dim slice per box), whole 64-token blocks
+    ("fp16", 64, 32, 4, 8, (30, 400)),    # d = 64, 8-token blocks, 8 query heads per kv head
 ]
 
 
