@@ -38,6 +38,37 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(pa.pagedattn.EXPORTED) <= set(names)
 
 
+def test_header_compiles_and_links_as_plain_c(lib, tmp_path):
+    # the boundary is a C ABI: the header compiles as C99 (no C++), and a C
+    # program links against the library and gets the same host-side answer
+    # as the Python binding (workspace sizing needs no GPU)
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    cuda_inc = None
+    for d in (os.environ.get("CUDA_HOME", ""), "/usr/local/cuda"):
+        if d and os.path.exists(os.path.join(d, "include", "cuda_runtime_api.h")):
+            cuda_inc = os.path.join(d, "include")
+            break
+    if gcc is None or cuda_inc is None:
+        pytest.skip("gcc or the CUDA headers are not available")
+    libdir = os.path.dirname(pbuild.LIB_PATH)
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "pagedattn.h"\n#include <stdio.h>\n'
+                   "int main(void) {\n"
+                   "  printf(\"%zu\\n\", pa_decode_workspace_bytes(4, 8, 128, 64, 16, 512));\n"
+                   "  return pa_last_error() == 0;\n"
+                   "}\n")
+    exe = tmp_path / "use_header"
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        "-I", cuda_inc, str(src), "-L", libdir, "-lpagedattn",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert out.returncode == 0, out.stderr
+    assert int(out.stdout.strip()) == pa.decode_workspace_bytes(4, 8, 128, 64, 16, 512)
+
+
 def test_library_is_built_for_sm_103a_only():
     assert pbuild.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
