@@ -635,7 +635,7 @@ def run_serving_step(args):
             pa.copy_blocks(kc, vc, c[0], c[1])
             copies_seen[0] += len(copies)
         pa.reshape_and_cache(nk, nv, kc, vc, slots_d)
-        pa.decode(out, q, kc, vc, bt, sl, None, 0, ws)
+        pa.decode(out, q, kc, vc, bt, sl, 1.0 / d ** 0.5, 0, ws)
         bytes_seen[0] += int(2 * lens.astype(np.int64).sum() * Hkv * d * 2)
 
     for _ in range(max(3, args.warmup)):

@@ -12,9 +12,12 @@
  *
  * Conventions shared by every entry point:
  *   - Every pointer argument is DEVICE memory owned by the caller, unless the
- *     parameter says otherwise. The library allocates nothing and keeps no
- *     state except a thread-local error string and one device-resident counter
- *     of rejected indices (see pa_bad_index_count).
+ *     parameter says otherwise. The library allocates nothing. Its state is a
+ *     thread-local error string, two device-resident counters (rejected
+ *     indices, see pa_bad_index_count; waits that gave up, see
+ *     pa_wait_timeout_count), a host-side note of which leading bytes of each
+ *     recently used split-K workspace are zero (see
+ *     pa_decode_workspace_bytes), and the fixed scratch of pa_decode_no_alloc.
  *   - Work is enqueued on `stream` and returns without synchronising. Inputs
  *     must stay valid until the stream reaches the work.
  *   - A negative return value means the call enqueued nothing (or, for
@@ -61,9 +64,9 @@ enum {
  * key_cache[slot / B, slot % B, :, :] and value_cache[...] bit for bit.
  * A negative slot skips token i. This is the write vLLM performs for the new
  * token before the attention kernel runs ("PagedAttention by hand", Setup,
- * Step 1; Code: "fused reshape and block write"); the slot of logical token t
- * of a sequence is table[t / B] * B + t % B ("The PagedAttention Algorithm":
- * logical token to "slot 9 in block 47").
+ * Step 1, and the Code section); the slot of logical token t of a sequence is
+ * table[t / B] * B + t % B ("The PagedAttention Algorithm", opening: a
+ * logical token maps to an offset inside a numbered physical block).
  *
  * Sizes: num_tokens >= 0 (0 is a no-op), num_kv_heads >= 1, head_dim in
  * {64, 128}, block_size a power of two in [1, 64], num_blocks >= 1.
@@ -83,11 +86,17 @@ int pa_reshape_and_cache(const void* key, const void* value,
  * partition_tokens is the value that will be passed to pa_decode (0 = the
  * library's default, 512 tokens). Returns 0 for invalid sizes.
  *
- * Workspace contents: per-(sequence, kv-head) arrival counters followed by
- * fp32 partial results. The counters must be ZERO before the first pa_decode
- * that uses a workspace; every pa_decode leaves them zero again when it
- * completes, so one zero-fill at allocation is enough. Calls that share a
- * workspace must not overlap on the GPU.
+ * Workspace contents: per-(sequence, kv-head) arrival counters at the start,
+ * followed by fp32 partial results. Zero-fill a new workspace once, at
+ * allocation. Every pa_decode leaves the counters it used at zero. When a
+ * later call's counters reach into bytes an earlier call on the same
+ * workspace used for partial results (more sequences or heads, or other
+ * sizes), pa_decode clears its counter region itself, with one
+ * cudaMemsetAsync on the call's stream; the library tracks this per workspace
+ * address, so distinct workspaces must not overlap in memory. A call captured
+ * in a CUDA graph replays without that check: between replays, use its
+ * workspace only with the captured sizes (or zero it again). Calls that share
+ * a workspace must not overlap on the GPU.
  */
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size,

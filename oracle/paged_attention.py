@@ -16,16 +16,16 @@ What it computes (sources are the three pages on PagedAttention):
   max-subtracted softmax (PagedAttention by hand, Forward pass, Step 3) and a
   probability-weighted sum of V (Step 4).
 * Logical token ``t`` lives in physical block ``table[t // B]`` at offset
-  ``t % B`` (The PagedAttention Algorithm, opening: logical "token 25" to
-  physical "slot 9 in block 47").
+  ``t % B`` (The PagedAttention Algorithm, opening: the example that maps a
+  token of a sequence to an offset inside a numbered physical block).
 * Only tokens ``t < seq_len`` exist; slots past it are never read
   (PagedAttention by hand, Step 2: bound the loop so invalid slots are never
   touched).
 * Inputs are fp16/bf16 bit patterns, widened exactly to float64.
 * The cache write puts token ``i``'s K/V row into ``slot_mapping[i]``
   (= physical block * B + offset; negative = skip), the step vLLM performs
-  before attention (PagedAttention by hand, Step 1; Code: "fused reshape and
-  block write").
+  before attention (PagedAttention by hand, Setup, Step 1, and the Code
+  section).
 * Split-K: attention over a token range gives (log-sum-exp, normalised
   output); ranges combine by log-sum-exp weights. This is the running
   max / running sum of the online softmax (The PagedAttention Algorithm,

@@ -7,7 +7,9 @@
 #include <stdio.h>
 
 #include <atomic>
+#include <mutex>
 #include <string>
+#include <vector>
 
 #include "internal.h"
 #include "pagedattn.h"
@@ -119,6 +121,47 @@ int resolve_partition(int partition_tokens, int block_size, int* pt) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Split-K workspaces: how many leading bytes of each are known to be zero.
+// Every pa_decode leaves the arrival counters it used at zero and writes fp32
+// partial results from lse_off on. A later call whose counters reach past the
+// known-zero prefix (more rows, or after a call whose partial results started
+// earlier) would find partial-result bytes there, so it clears its counter
+// region on the stream first. Kept per workspace address, most recent last; an
+// address not in the list counts as unknown and is cleared once.
+struct WsZero {
+  const void* ptr;
+  size_t zero_prefix;
+};
+std::mutex g_ws_mu;
+std::vector<WsZero> g_ws_zero;
+constexpr size_t kWsRecords = 64;
+
+// Clears [0, lse_off) of `ws` on `stream` unless its counters
+// [0, counter_bytes) are already known to be zero; records the zero prefix
+// this call leaves behind.
+cudaError_t prepare_workspace(void* ws, size_t counter_bytes, size_t lse_off,
+                              cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  size_t zp = 0;
+  size_t i = 0;
+  for (; i < g_ws_zero.size(); ++i)
+    if (g_ws_zero[i].ptr == ws) break;
+  if (i < g_ws_zero.size()) {
+    zp = g_ws_zero[i].zero_prefix;
+    g_ws_zero.erase(g_ws_zero.begin() + static_cast<long>(i));
+  }
+  if (counter_bytes > zp) {
+    cudaError_t e = cudaMemsetAsync(ws, 0, lse_off, stream);
+    if (e != cudaSuccess) return e;
+    zp = lse_off;
+  } else if (lse_off < zp) {
+    zp = lse_off;  // this call's partial results start inside the old prefix
+  }
+  if (g_ws_zero.size() >= kWsRecords) g_ws_zero.erase(g_ws_zero.begin());
+  g_ws_zero.push_back({ws, zp});
+  return cudaSuccess;
+}
 
 }  // namespace
 
@@ -373,6 +416,11 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
   unsigned long long* bad = nullptr;
   rc = bad_counter(&bad);
   if (rc != PA_OK) return rc;
+  if (wl.total > 0) {
+    const size_t counter_bytes = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int);
+    cudaError_t e = prepare_workspace(workspace, counter_bytes, wl.lse_off, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
+  }
 
   pa::DecodeArgs a{};
   a.out = out;

@@ -1,7 +1,7 @@
 // Cache write: copy each new token's K and V rows into its slot of the paged
 // pool. vLLM performs this write for the token being decoded before the
-// attention kernel runs ("PagedAttention by hand", Setup, Step 1; Code:
-// "fused reshape and block write"). With the [blocks, B, Hkv, d] layout the
+// attention kernel runs ("PagedAttention by hand", Setup, Step 1, and the
+// Code section). With the [blocks, B, Hkv, d] layout the
 // [Hkv, d] rows of one token are contiguous both in the source and at the
 // slot, so the copy is one contiguous run of Hkv * d * 2 bytes per tensor,
 // moved in 16-byte vectors.

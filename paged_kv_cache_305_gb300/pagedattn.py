@@ -9,7 +9,6 @@ fallback path.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 from typing import Optional
 
@@ -162,12 +161,13 @@ def alloc_workspace(query: torch.Tensor, key_cache: torch.Tensor, block_tables: 
 
 def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
            value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
-           scale: Optional[float] = None, partition_tokens: int = 0,
+           scale: float, partition_tokens: int = 0,
            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Paged decode attention into ``out`` [S, Hq, d]; returns ``out``.
 
     ``query`` [S, Hq, d]; caches [NB, B, Hkv, d]; ``block_tables`` [S, MB]
-    int32; ``seq_lens`` [S] int32. ``scale`` defaults to 1/sqrt(d). ``out``
+    int32; ``seq_lens`` [S] int32. ``scale`` multiplies q.K (the caller's
+    choice; the library has no default, e.g. 1/sqrt(d) for standard attention). ``out``
     has the query's dtype (rounded result) or float32 (the result before that
     rounding). The workspace, when one is needed, comes from
     :func:`alloc_workspace` (zeroed once, reusable across calls on one stream).
@@ -183,8 +183,6 @@ def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
           "block_tables/seq_lens shape mismatch")
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     ws_ptr, ws_bytes = 0, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
@@ -202,7 +200,7 @@ def decode(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
 
 def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
                   new_value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
-                  block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: Optional[float] = None,
+                  block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
                   partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
                   stream=None) -> torch.Tensor:
     """:func:`decode` that also writes each sequence's newest token (position
@@ -223,8 +221,6 @@ def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
           "block_tables/seq_lens shape mismatch")
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     ws_ptr, ws_bytes = 0, 0
     if workspace is not None:
         ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
@@ -242,7 +238,7 @@ def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
 
 def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
             value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
-            query_start: torch.Tensor, max_query_len: int, scale: Optional[float] = None,
+            query_start: torch.Tensor, max_query_len: int, scale: float,
             stream=None) -> torch.Tensor:
     """Causal attention of each sequence's newest tokens over the paged cache.
 
@@ -262,8 +258,6 @@ def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
     _need(block_tables.shape[0] == S and query_start.shape == (S + 1,), "shape mismatch")
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens, query_start):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     L = load_library()
     with torch.cuda.device(query.device):
         _check(L.pa_prefill(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
@@ -291,7 +285,7 @@ def wait_timeout_count(clear: bool = False) -> int:
 
 def decode_no_alloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                     value_cache: torch.Tensor, block_tables: torch.Tensor,
-                    seq_lens: torch.Tensor, scale: Optional[float] = None,
+                    seq_lens: torch.Tensor, scale: float,
                     partition_tokens: int = 0, stream=None) -> torch.Tensor:
     """:func:`decode` for callers that cannot allocate device memory.
 
@@ -311,8 +305,6 @@ def decode_no_alloc(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
           "block_tables/seq_lens shape mismatch")
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
-    if scale is None:
-        scale = 1.0 / math.sqrt(d)
     L = load_library()
     with torch.cuda.device(query.device):
         _check(L.pa_decode_no_alloc(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),

@@ -206,6 +206,36 @@ def test_repeatable_and_workspace_reusable():
     assert np.array_equal(_parity(dc, ref), a)
 
 
+def test_one_workspace_for_a_small_then_a_larger_batch():
+    # A serving loop whose batch grows keeps its workspace: the larger call's
+    # arrival counters then sit on bytes where the smaller call left fp32
+    # partial results (its log-sum-exp values start right after its 64
+    # counters). Every row of both calls is cut into pieces (many 16- or
+    # 64-token partitions per row), so every row goes through a counter.
+    small = W.random_case(num_seqs=2, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                          len_range=(2500, 3000), dtype="bf16", seed=31, partition_tokens=16)
+    big = W.random_case(num_seqs=40, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                        len_range=(2500, 3000), dtype="bf16", seed=32, partition_tokens=64)
+    cases = [DeviceCase(c) for c in (small, big)]
+    need = max(pa.decode_workspace_bytes(c.num_seqs, c.num_q_heads, c.head_dim,
+                                         c.max_blocks_per_seq, c.block_size, c.partition_tokens)
+               for c in (small, big))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    refs = [oracle.paged_decode(c.query, c.key_cache, c.value_cache, c.block_tables, c.seq_lens,
+                                c.block_size, c.scale, c.dtype) for c in (small, big)]
+    for k in (0, 1, 0, 1):
+        dc, c = cases[k], cases[k].case
+        got = []
+        for out in (dc.out, dc.out32):
+            out.fill_(float("nan"))  # a row the merge never writes stays NaN
+            pa.decode(out, dc.query, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens,
+                      c.scale, c.partition_tokens, ws)
+            got.append(out.clone())
+        check_parity(host_bits(got[0]), got[1].cpu().numpy(), refs[k], c.dtype,
+                     f"shared workspace, call with {c.num_seqs} sequences")
+        assert np.array_equal(got[1].cpu().numpy(), dc.decode(out_f32=True).cpu().numpy())
+
+
 def test_partition_length_does_not_change_the_result():
     case = W.random_case(num_seqs=4, num_q_heads=8, num_kv_heads=1, head_dim=128, block_size=16,
                          len_range=(2000, 5000), dtype="bf16", seed=7)

@@ -5,8 +5,9 @@
   blocks of 2 shared by two candidates; the first candidate to write token 6
   copies only the last block, the second writes in place, the first two blocks
   stay shared with a reference count of 2;
-* the glossary's "a new physical block is allocated only when the previous one
-  fills" and the by-hand page's waste bound of at most B - 1 slots per sequence;
+* the glossary's rule that a sequence gets a new physical block only once its
+  previous block is full, and the by-hand page's waste bound of at most B - 1
+  slots per sequence;
 * invariants recomputed from the tables by brute force: reference counts equal
   the number of tables holding a block, free + used blocks = pool size.
 """

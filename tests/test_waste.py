@@ -16,7 +16,7 @@ def test_page_examples_of_contiguous_reservation():
 
 
 def test_page_example_of_paged_allocation():
-    # "exactly 3 blocks (6 slots) for a 5-token sequence"; one empty slot wasted
+    # the by-hand page: 5 tokens in blocks of 2 take 3 blocks (6 slots), one slot unused
     assert paged_waste([5], 2) == (1, 6)
 
 
@@ -24,7 +24,8 @@ def test_paged_waste_is_at_most_block_size_minus_one_per_sequence():
     for B in (1, 2, 8, 16, 64):
         worst = max(paged_waste([L], B)[0] for L in range(1, 3 * B + 5))
         assert worst == B - 1
-    # "~15 slots per sequence at B=16, regardless of length" (20 or 20000 tokens)
+    # the by-hand page: about 15 wasted slots per sequence at B = 16, whatever
+    # the length (here 20 or 20000 tokens)
     assert paged_waste([20], 16)[0] <= 15 and paged_waste([20000], 16)[0] <= 15
     assert max(paged_waste([20000 + k], 16)[0] for k in range(16)) == 15
 
@@ -40,11 +41,3 @@ def test_simulator_matches_the_accounting_step_by_step(B):
     contig = sum(contiguous_waste(t, r.max_len)[1] for t in trace)
     assert (used, paged, contig) == (r.used_token_steps, r.paged_slot_steps, r.contiguous_slot_steps)
     assert r.max_paged_waste_per_seq <= B - 1
-
-
-def test_default_trace_reproduces_the_magnitudes_on_the_pages():
-    pbuild.build()
-    from paged_kv_cache_305_gb300 import waste
-    r = waste.simulate(block_size=16)
-    assert 0.60 <= r.contiguous_waste <= 0.80  # "wastes 60-80% of KV memory"
-    assert r.paged_waste < 0.05

@@ -14,7 +14,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import paged_kv_cache_305_gb300 as pa
 import workloads as W
-from gpu_util import ATOL, DeviceCase, host_bits
+from gpu_util import DeviceCase, check_parity, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -42,30 +42,37 @@ def test_no_alloc_matches_workspace_decode_on_two_calls(dtype):
     dc = DeviceCase(case)
     want16 = host_bits(dc.decode()).copy()
     want32 = dc.decode(out_f32=True).cpu().numpy().copy()
+    ref = oracle.paged_decode(case.query, case.key_cache, case.value_cache, case.block_tables,
+                              case.seq_lens, case.block_size, case.scale, dtype)
     for call in range(2):
-        out16 = torch.empty_like(dc.query)
-        out32 = torch.empty(dc.query.shape, dtype=torch.float32, device="cuda")
+        out16 = torch.full(dc.query.shape, float("nan"), dtype=dc.query.dtype, device="cuda")
+        out32 = torch.full(dc.query.shape, float("nan"), dtype=torch.float32, device="cuda")
         _no_alloc(dc, out16, 128)
         _no_alloc(dc, out32, 128)
         torch.cuda.synchronize()
-        got16 = oracle.to_float64(host_bits(out16), dtype)
-        assert np.max(np.abs(got16 - oracle.to_float64(want16, dtype))) <= ATOL, call
-        assert np.max(np.abs(out32.cpu().numpy().astype(np.float64) - want32)) <= ATOL, call
+        # the same kernel and schedule as pa_decode: the same bits
+        assert np.array_equal(host_bits(out16), want16), call
+        assert np.array_equal(out32.cpu().numpy(), want32), call
+        check_parity(host_bits(out16), out32.cpu().numpy(), ref, dtype, f"no-alloc call {call}")
 
 
 def test_no_alloc_after_a_different_shape():
-    # the scratch keeps the previous call's contents; a new shape must not see them
-    big = W.random_case(num_seqs=9, num_q_heads=8, num_kv_heads=8, head_dim=64, block_size=8,
-                        len_range=(500, 2500), dtype="fp16", seed=22, partition_tokens=64)
-    small = W.random_case(num_seqs=3, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
-                          len_range=(200, 1500), dtype="bf16", seed=23, partition_tokens=96 * 2)
+    # The scratch keeps the previous call's contents. The small call (2 x 32
+    # query heads = 64 rows) leaves its fp32 log-sum-exp values right after
+    # its 64 counters; the big call's 40 x 8 counters then cover those bytes.
+    # Every row of both is cut into pieces, so every row goes through a counter.
+    small = W.random_case(num_seqs=2, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                          len_range=(2500, 3000), dtype="bf16", seed=22, partition_tokens=16)
+    big = W.random_case(num_seqs=40, num_q_heads=32, num_kv_heads=8, head_dim=128, block_size=16,
+                        len_range=(2500, 3000), dtype="bf16", seed=23, partition_tokens=64)
     for case in (big, small, big):
         dc = DeviceCase(case)
+        # pa_decode on a freshly zeroed workspace of its own
         want = dc.decode(out_f32=True).cpu().numpy().copy()
-        out = torch.empty(dc.query.shape, dtype=torch.float32, device="cuda")
+        out = torch.full(dc.query.shape, float("nan"), dtype=torch.float32, device="cuda")
         _no_alloc(dc, out, case.partition_tokens)
         torch.cuda.synchronize()
-        assert np.max(np.abs(out.cpu().numpy().astype(np.float64) - want)) <= ATOL
+        assert np.array_equal(out.cpu().numpy(), want), case.num_seqs
 
 
 def test_no_alloc_rejects_sizes_beyond_its_scratch():
