@@ -1,12 +1,11 @@
 """Full-size workloads on the GPU, in the launch configuration bench.py times.
 
-The oracle computes sampled (sequence, query head) output rows one by one;
-every output row is also checked for properties that hold at any size
-(finite; within the range of the V rows it averages). The step: write each
-sequence's newest token with pa_reshape_and_cache, then pa_decode over the
-whole sequence; and, where every newest token has a block of its own, the
-fused pa_decode_append that the benchmark times by default, which must give
-the same bits.
+Every (sequence, query head) output row of every workload is compared with
+the float64 oracle (fp32 result within 2e-3, 16-bit output its nearest-even
+rounding). The step: write each sequence's newest token with
+pa_reshape_and_cache, then pa_decode over the whole sequence; and, where
+every newest token has a block of its own, the fused pa_decode_append that
+the benchmark times by default, which must give the same bits.
 """
 import numpy as np
 import pytest
@@ -16,7 +15,7 @@ torch = pytest.importorskip("torch")
 import oracle
 import paged_kv_cache_305_gb300 as pa
 import workloads as W
-from gpu_util import ATOL, DeviceCase, check_parity, host_bits
+from gpu_util import DeviceCase, check_parity, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -30,20 +29,6 @@ def _cuda():
     yield
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-
-
-def _pairs(case, n_random=40, seed=0):
-    rng = np.random.default_rng(seed)
-    L = case.seq_lens
-    seqs = {int(np.argmax(L)), int(np.argmin(L)), int(np.argsort(L)[len(L) // 2])}
-    Hq, G = case.num_q_heads, case.group
-    pairs = set()
-    for s in seqs:
-        for hq in {0, G - 1, Hq - 1, int(rng.integers(Hq))}:
-            pairs.add((s, hq))
-    while len(pairs) < len(seqs) * 4 + n_random:
-        pairs.add((int(rng.integers(case.num_seqs)), int(rng.integers(Hq))))
-    return sorted(pairs)
 
 
 def _run_and_check(case):
@@ -73,17 +58,11 @@ def _run_and_check(case):
                                       case.value_cache, case.slot_mapping, B, in_place=True)
     del dc
     torch.cuda.empty_cache()
-    pairs = _pairs(case)
-    ref = oracle.paged_decode_pairs(case.query, kc, vc, case.block_tables, case.seq_lens, B,
-                                    case.scale, case.dtype, pairs)
-    sel16 = np.stack([got[s, h] for s, h in pairs])
-    sel32 = np.stack([got32[s, h] for s, h in pairs])
-    err = check_parity(sel16, sel32, ref, case.dtype, f"{case.name} ({len(pairs)} sampled rows)")
-    full = oracle.to_float64(got, case.dtype)
-    assert np.all(np.isfinite(full))
-    vmax = float(np.max(np.abs(oracle.to_float64(case.value_cache[:: max(1, case.num_blocks // 64)],
-                                                 case.dtype))))
-    assert np.max(np.abs(full)) <= max(vmax, 8.0)
+    # the oracle over the whole batch: every row, every head
+    ref = oracle.paged_decode(case.query, kc, vc, case.block_tables, case.seq_lens, B,
+                              case.scale, case.dtype)
+    err = check_parity(got, got32, ref, case.dtype,
+                       f"{case.name} (all {case.num_seqs * case.num_q_heads} rows)")
     return err
 
 
