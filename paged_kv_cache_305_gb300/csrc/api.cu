@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "pagedattn.h"
+#include "pagedattn_testing.h"
 
 namespace {
 
@@ -256,11 +257,15 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int32_t* src, const
   return PA_OK;
 }
 
-int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
-               const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
-               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-               float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
-               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+int prefill_impl(void* out, const void* query, const void* key_cache, const void* value_cache,
+                 const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
+                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                 float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
+                 pa_dtype dtype, pa_dtype out_dtype, int stall_for_test, cudaStream_t stream) {
   g_error.clear();
   int rc = check_dtype(dtype);
   if (rc != PA_OK) return rc;
@@ -317,11 +322,38 @@ int pa_prefill(void* out, const void* query, const void* key_cache, const void* 
   a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
   a.bad = bad;
+  a.stall_for_test = stall_for_test;
   rc = counter(true, &a.timeouts);
   if (rc != PA_OK) return rc;
   cudaError_t e = pa::launch_prefill_tc(a, head_dim, dtype == PA_BFLOAT16, max_query_len, stream);
   if (e != cudaSuccess) return cuda_fail(e, "paged prefill launch");
   return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
+               const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
+               int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+               float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
+               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream) {
+  return prefill_impl(out, query, key_cache, value_cache, block_tables, seq_lens, query_start,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, 0, stream);
+}
+
+int pa_testing_prefill_stalled(void* out, const void* query, const void* key_cache,
+                               const void* value_cache, const int32_t* block_tables,
+                               const int32_t* seq_lens, const int32_t* query_start, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               float scale, int max_blocks_per_seq, int num_blocks,
+                               int max_query_len, pa_dtype dtype, pa_dtype out_dtype,
+                               cudaStream_t stream) {
+  return prefill_impl(out, query, key_cache, value_cache, block_tables, seq_lens, query_start,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale,
+                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, 1, stream);
 }
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,

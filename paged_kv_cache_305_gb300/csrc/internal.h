@@ -57,6 +57,7 @@ struct PrefillArgs {
   int out_f32;
   unsigned long long* bad;
   unsigned long long* timeouts;  // bounded waits that gave up (tensor-core kernel)
+  int stall_for_test;  // 1: the product thread waits on a barrier nothing signals
 };
 
 // Tensor-core (tcgen05) prefill: block sizes 1..64 (TMA block copies from 8

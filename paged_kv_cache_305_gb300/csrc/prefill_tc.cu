@@ -97,6 +97,7 @@ enum : int {
   kBarODone = 8,   // [2] P_j V done: O updated, V stage and P columns free
   kBarQFull = 10,  // query tile in shared memory
   kTmemSlot = 11,  // 4-byte TMEM base address
+  kBarNever = 12,  // nothing arrives here: the wait of a stalled test launch
 };
 
 // Offset of 16-byte chunk (chunk & 7) of row `row` inside one 128-byte-row
@@ -203,6 +204,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     tc::mbar_init(bar(kBarPFull), 128);
     tc::mbar_init(bar(kBarSFree), 128);
     tc::mbar_init(bar(kBarQFull), 128);
+    tc::mbar_init(bar(kBarNever), 1);
     tc::mbar_init_fence();
   }
   if (warp == 0) tc::tmem_alloc(bar(kTmemSlot), kTmemCols);
@@ -580,7 +582,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       tc::tc_commit(bar(kBarSFull + st));
     };
     uint32_t last_bar = 0, last_parity = 0;  // the latest commit
-    ok = tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
+    // a stalled test launch first waits on a barrier that nothing signals:
+    // the wait runs out, no product is issued, and every warp winds down
+    if (a.stall_for_test) ok = tc::mbar_wait(bar(kBarNever), 0);
+    ok = ok && tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
     if (ok) {
       tc::tc_fence_after();
       if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products

@@ -23,7 +23,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_decode_no_alloc_scratch_bytes", "pa_copy_blocks", "pa_bm_create",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
             "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
-            "pa_decode_append", "pa_prefill", "pa_wait_timeout_count")
+            "pa_decode_append", "pa_prefill", "pa_wait_timeout_count",
+            "pa_testing_prefill_stalled")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -70,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
                              i32, i32, i32, i32, i32, vp]
     L.pa_prefill.restype = i32
+    L.pa_testing_prefill_stalled.argtypes = L.pa_prefill.argtypes
+    L.pa_testing_prefill_stalled.restype = i32
     L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     L.pa_copy_blocks.restype = i32
     ip = ctypes.POINTER(ctypes.c_int)
@@ -236,17 +239,10 @@ def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
     return out
 
 
-def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+def _prefill(entry, out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
             value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
             query_start: torch.Tensor, max_query_len: int, scale: float,
             stream=None) -> torch.Tensor:
-    """Causal attention of each sequence's newest tokens over the paged cache.
-
-    ``query``/``out`` [total_q, Hq, d]; sequence s owns query rows
-    query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its newest tokens,
-    whose K/V are already in the cache; ``max_query_len`` bounds the rows per
-    sequence.
-    """
     total_q, Hq, d = query.shape
     NB, B, Hkv, d2 = key_cache.shape
     S = seq_lens.shape[0]
@@ -260,13 +256,39 @@ def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
     L = load_library()
     with torch.cuda.device(query.device):
-        _check(L.pa_prefill(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
-                            value_cache.data_ptr(), block_tables.data_ptr(), seq_lens.data_ptr(),
-                            query_start.data_ptr(), S, Hq, Hkv, d, B, float(scale),
-                            block_tables.shape[1], NB, int(max_query_len), _dtype_code(query),
-                            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
-                            _stream(query, stream)))
+        _check(getattr(L, entry)(
+            out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+            block_tables.data_ptr(), seq_lens.data_ptr(), query_start.data_ptr(), S, Hq, Hkv, d, B,
+            float(scale), block_tables.shape[1], NB, int(max_query_len), _dtype_code(query),
+            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+            _stream(query, stream)))
     return out
+
+
+def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+            value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+            query_start: torch.Tensor, max_query_len: int, scale: float,
+            stream=None) -> torch.Tensor:
+    """Causal attention of each sequence's newest tokens over the paged cache.
+
+    ``query``/``out`` [total_q, Hq, d]; sequence s owns query rows
+    query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its newest tokens,
+    whose K/V are already in the cache; ``max_query_len`` bounds the rows per
+    sequence.
+    """
+    return _prefill("pa_prefill", out, query, key_cache, value_cache, block_tables, seq_lens,
+                    query_start, max_query_len, scale, stream)
+
+
+def testing_prefill_stalled(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                            value_cache: torch.Tensor, block_tables: torch.Tensor,
+                            seq_lens: torch.Tensor, query_start: torch.Tensor, max_query_len: int,
+                            scale: float, stream=None) -> torch.Tensor:
+    """Test hook (include/pagedattn_testing.h): :func:`prefill` whose product
+    thread waits on a barrier nothing signals, so bounded waits give up and
+    the launch winds down; ``out`` is left unwritten."""
+    return _prefill("pa_testing_prefill_stalled", out, query, key_cache, value_cache,
+                    block_tables, seq_lens, query_start, max_query_len, scale, stream)
 
 
 def bad_index_count(clear: bool = False) -> int:

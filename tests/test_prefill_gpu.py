@@ -202,3 +202,30 @@ def test_full_size_chunked_prefill_sampled():
             ref, _ = oracle.single_query_attention(qrow, K[:pos + 1, h], V[:pos + 1, h], case.scale)
             err = max(err, float(np.max(np.abs(got32[starts[s] + j, h * G:(h + 1) * G] - ref))))
     assert err <= ATOL, f"full-size prefill: max |fp32 - oracle| over sampled rows = {err}"
+
+
+@pytest.mark.parametrize("B", [16, 4])
+def test_a_wait_that_runs_out_is_counted_and_the_device_stays_usable(B):
+    # The test hook makes each CTA's product thread wait on a barrier that
+    # nothing signals: that bounded wait gives up (about one second), the
+    # warps waiting for products give up after it, and every CTA winds down.
+    # The call must return, the give-ups must be counted, and the next normal
+    # call on the same device must give the bits of a fresh run.
+    case = W.random_case(num_seqs=2, num_q_heads=8, num_kv_heads=2, head_dim=128, block_size=B,
+                         len_range=(150, 300), dtype="bf16", seed=60 + B)
+    qlens = [int(case.seq_lens[0]), 70]
+    q0, fresh = _run(case, qlens, 13)
+    starts = torch.from_numpy(np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)).cuda()
+    dc = DeviceCase(case)
+    qd = dev_bits(q0, "bf16")
+    pa.wait_timeout_count(clear=True)
+    stalled = torch.full(qd.shape, 7.0, dtype=torch.float32, device="cuda")
+    pa.testing_prefill_stalled(stalled, qd, dc.key_cache, dc.value_cache, dc.block_tables,
+                               dc.seq_lens, starts, max(qlens), case.scale)
+    assert pa.wait_timeout_count(clear=True) >= 1
+    assert bool((stalled == 7.0).all())  # no product ran, nothing was stored
+    out = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
+    pa.prefill(out, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, starts,
+               max(qlens), case.scale)
+    assert np.array_equal(out.cpu().numpy(), fresh)
+    assert pa.wait_timeout_count(clear=True) == 0
