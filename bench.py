@@ -190,11 +190,29 @@ def time_oracle(case, budget_s: float, start: int = 0):
     return nbytes / dt / 1e9, dt, done
 
 
+def host_cores() -> int:
+    """Cores this process may run on (the machine's host cores available to the run)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# Why the oracle runs on one thread: it is timed as it stands, a plain NumPy
+# program whose work per output row is small matrix-vector products (a few
+# heads against a few thousand keys), where extra BLAS threads add overhead
+# rather than speed; rows are independent, so a run over all host cores would
+# take about the one-thread time divided by the core count.
+ONE_THREAD = ("the oracle as it stands is single-threaded NumPy (BLAS pinned to 1 thread: "
+              "per output row it does small matrix-vector products); its rows are independent")
+
+
 def cpu_baseline_block(case, budget_s):
     t0 = time.perf_counter()
     oracle_prepare(case)
     gbs, dt, done = time_oracle(case, budget_s)
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "host_cores": host_cores(),
+            "kind": "oracle", "why_one_thread": ONE_THREAD,
             "sample": f"float64 NumPy oracle (one thread): {done} of {case.num_seqs * case.num_q_heads} "
                       f"(sequence, query head) output rows of the same batch in {dt:.1f} s "
                       f"(after its cache write, {time.perf_counter() - t0 - dt:.1f} s)"}
@@ -219,13 +237,20 @@ def run_reference(args, rank, world):
         tot_bytes += gbs * dt * 1e9
         tot_s += dt
     gbs = tot_bytes / tot_s / 1e9
+    S_Hq = case.num_seqs * case.num_q_heads
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        # each timed step is a bounded sample of the step's output rows
         "ms_per_step": round(1e3 * tot_s / args.steps, 3),
+        "ms_per_step_kind": f"sample: {rows / args.steps:.0f} of the step's {S_Hq} (sequence, "
+                            f"query head) output rows per timed step; value = the sampled rows' "
+                            f"algorithmic bytes / their time",
+        "ms_per_whole_step_estimate": round(1e3 * tot_s / args.steps * S_Hq / max(1.0, rows / args.steps), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
         "data": "synthetic", "config": _config(case, args),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1,
+                         "host_cores": host_cores(), "kind": "oracle", "why_one_thread": ONE_THREAD,
                          "sample": f"float64 NumPy oracle (one thread): {rows} (sequence, query head) "
                                    f"output rows over {args.steps} steps of ~{per_step:.3f} s each"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -240,8 +265,12 @@ def _config(case, args):
             "block_size": case.block_size, "seq_len_range": [int(case.seq_lens.min()),
                                                              int(case.seq_lens.max())],
             "mean_seq_len": round(float(case.seq_lens.mean()), 1),
-            "partition_tokens": args.partition_tokens or 512,
+            "partition_tokens": (args.partition_tokens if args.partition_tokens is not None
+                                 else case.partition_tokens) or 512,
             "kv_bytes_per_step": case.kv_bytes(),
+            "step": "write each sequence's newest K/V row into its slot, then decode attention "
+                    "over every sequence",
+            "cuda_graph": bool(getattr(args, "graph", False)),
             "l2": "no flush: inputs larger than L2 (KV read per step >> 129 MB)",
             "parallelism": "replicas (weak scaling, no collective)", "seed": 0}
 
@@ -322,8 +351,9 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     barrier()
-    with ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
-                      int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])) as clk:
+    gpu_index = (local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                 int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank]))
+    with ClockSampler(gpu_index) as clk:
         start.record(stream)
         for i in range(K):
             if graph is not None:
@@ -447,13 +477,11 @@ def run_ours(args, rank, world, local_rank):
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
         "data": "synthetic",
-        "config": _config(case, args) | {"partition_tokens": pt or 512,
-                                         "step": "pa_decode_append (one kernel)" if fused else
-                                                 "pa_reshape_and_cache + pa_decode" +
-                                                 ("" if fused_ok or args.step != "fused" else
-                                                  " (some newest tokens sit in shared blocks: "
-                                                  "the fused write does not apply)"),
-                                         "cuda_graph": bool(args.graph)},
+        "config": _config(case, args),
+        "step_impl": "pa_decode_append (one kernel)" if fused else
+                     "pa_reshape_and_cache + pa_decode" +
+                     ("" if fused_ok or args.step != "fused" else
+                      " (some newest tokens sit in shared blocks: the fused write does not apply)"),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         **({"unique_kv_bytes_per_step": case.unique_kv_bytes(),
             "unique_kv_GBps": round(case.unique_kv_bytes() * K * world / (ms * 1e-3) / 1e9, 2)}
@@ -474,6 +502,9 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": K if fused else 2 * K,
         "clocks": clk.summary(),
     }
+    if not args.no_prefill:
+        # measured after the decode's timed region, on the same GPU
+        line["prefill"] = prefill_block(max(10, min(K, 50)), max(3, args.warmup), gpu_index)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_block(
             W.make_workload(args.workload, seed=0, block_size=args.block_size,
@@ -674,15 +705,21 @@ def run_waste(args):
                                  "prompt_range": [16, 512], "output": "geometric, mean 200", "seed": 0}}))
 
 
-def run_prefill(args):
-    """Paged causal prefill: algorithmic TFLOP/s (4 * d * Hq per causal pair)."""
+def _bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured bf16_tflops (cuBLAS, burst)"
+    return 1900.0, "fallback bf16 burst"
+
+
+def measure_prefill(ctx, chunk, B, tname, steps, warmup, S=16, Hq=32, Hkv=8, d=128):
+    """Paged causal prefill of S sequences (Hq/Hkv heads, head_dim d, block size
+    B): a chunk of `chunk` new tokens per sequence whose K/V are in the cache
+    after ctx - chunk older tokens (ctx = chunk: whole prompts). Returns
+    algorithmic TFLOP/s (4 * d * Hq flops per visible (query, key) pair) and
+    the CUDA-event time per call."""
     import torch
     import paged_kv_cache_305_gb300 as pa
-    from paged_kv_cache_305_gb300 import build as pbuild
-    pbuild.build()
-    S, Hq, Hkv, d, B = 16, 32, 8, 128, args.prefill_block_size
-    ctx, chunk = args.prefill_context, args.prefill_chunk
-    tname = args.prefill_dtype
     case = W.random_case(num_seqs=S, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
                          len_range=(ctx, ctx), dtype=tname, seed=0)
     dt = {"bf16": torch.bfloat16, "fp16": torch.float16}[tname]
@@ -694,21 +731,44 @@ def run_prefill(args):
     q = torch.randn((S * chunk, Hq, d), device="cuda").to(dt)
     out = torch.empty_like(q)
     ms = _events(lambda: pa.prefill(out, q, kc, vc, bt, sl, starts, chunk, case.scale),
-                 args.steps, max(3, args.warmup))
+                 steps, max(3, warmup))
     pairs = S * sum(ctx - chunk + j + 1 for j in range(chunk))
-    flops = 4.0 * d * Hq * pairs
-    tf = flops / (ms * 1e-3) / 1e12
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    # fp16 and bf16 products run at the same dense tensor rate
-    peak = float(json.load(open(p))["bf16_tflops"]) if os.path.exists(p) else 1900.0
+    tf = 4.0 * d * Hq * pairs / (ms * 1e-3) / 1e12
+    peak, kind = _bf16_peak()
+    del kc, vc, q, out
+    torch.cuda.empty_cache()
+    return {"value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+            "frac": round(tf / peak, 4), "tokens_per_s": round(S * chunk / (ms * 1e-3), 1),
+            "config": {"sequences": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
+                       "block_size": B, "context": ctx, "chunk": chunk, "dtype": tname}}
+
+
+def prefill_block(steps, warmup, gpu_index):
+    """The prefill sub-object of the default line: 2048-token chunks after 2048
+    cached tokens, and whole 2048-token prompts (bf16, block size 16)."""
+    peak, kind = _bf16_peak()
+    with ClockSampler(gpu_index) as clk:
+        chunked = measure_prefill(4096, 2048, 16, "bf16", steps, warmup)
+        whole = measure_prefill(2048, 2048, 16, "bf16", steps, warmup)
+    return {"kernel": "paged_prefill_tc_kernel", "metric": "paged causal prefill TFLOP/s (algorithmic)",
+            "bound": "tensor", "peak": peak, "peak_kind": kind, "chunked": chunked,
+            "whole_prompt": whole, "steps": steps, "launches_timed": 2 * steps,
+            "clocks": clk.summary()}
+
+
+def run_prefill(args):
+    """Paged causal prefill: algorithmic TFLOP/s (4 * d * Hq per causal pair)."""
+    from paged_kv_cache_305_gb300 import build as pbuild
+    pbuild.build()
+    r = measure_prefill(args.prefill_context, args.prefill_chunk, args.prefill_block_size,
+                        args.prefill_dtype, args.steps, args.warmup)
+    peak, kind = _bf16_peak()
     print(json.dumps({"op": "prefill", "metric": "paged causal prefill TFLOP/s (algorithmic)",
-                      "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
-                      "roofline": {"bound": "tensor", "achieved": round(tf, 1), "peak": peak,
-                                   "peak_kind": "measured bf16_tflops (cuBLAS, burst; fp16 has the same nominal rate)",
-                                   "frac": round(tf / peak, 4)},
-                      "tokens_per_s": round(S * chunk / (ms * 1e-3), 1), "steps": args.steps,
-                      "config": {"sequences": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
-                                 "block_size": B, "context": ctx, "chunk": chunk, "dtype": tname}}))
+                      "value": r["value"], "unit": "TFLOP/s", "ms_per_call": r["ms_per_call"],
+                      "roofline": {"bound": "tensor", "achieved": r["value"], "peak": peak,
+                                   "peak_kind": kind + "; fp16 has the same nominal rate",
+                                   "frac": r["frac"]},
+                      "tokens_per_s": r["tokens_per_s"], "steps": args.steps, "config": r["config"]}))
 
 
 def main():
@@ -727,6 +787,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="leave the prefill sub-object out of the default line")
     ap.add_argument("--prefill-context", type=int, default=4096)
     ap.add_argument("--prefill-chunk", type=int, default=2048)
     ap.add_argument("--prefill-block-size", type=int, default=16)
