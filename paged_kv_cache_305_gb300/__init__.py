@@ -22,5 +22,6 @@ from .pagedattn import (  # noqa: F401
     prefill,
     no_alloc_scratch_bytes,
     reshape_and_cache,
+    testing_prefill_stalled,
     wait_timeout_count,
 )

@@ -90,8 +90,9 @@ def test_serving_loop_with_forks_and_copy_on_write(dtype, B, Hq, Hkv, d):
         bt = torch.from_numpy(tables).cuda()
         sl = torch.from_numpy(lens).cuda()
         ws = pa.alloc_workspace(out16, kc, bt, 32)
-        pa.decode(out16, dev_bits(q, dtype), kc, vc, bt, sl, None, 32, ws)
-        pa.decode(out32, dev_bits(q, dtype), kc, vc, bt, sl, None, 32, ws)
+        scale = 1 / np.sqrt(d)
+        pa.decode(out16, dev_bits(q, dtype), kc, vc, bt, sl, scale, 32, ws)
+        pa.decode(out32, dev_bits(q, dtype), kc, vc, bt, sl, scale, 32, ws)
         G = Hq // Hkv
         ref = np.zeros((len(live), Hq, d))
         for i, s in enumerate(live):
@@ -99,7 +100,7 @@ def test_serving_loop_with_forks_and_copy_on_write(dtype, B, Hq, Hkv, d):
             V = oracle.to_float64(np.stack([r[1] for r in hist[s]]), dtype)
             qf = oracle.to_float64(q[i], dtype)
             for h in range(Hkv):
-                o, _ = oracle.single_query_attention(qf[h * G:(h + 1) * G], K[:, h], V[:, h], 1 / np.sqrt(d))
+                o, _ = oracle.single_query_attention(qf[h * G:(h + 1) * G], K[:, h], V[:, h], scale)
                 ref[i, h * G:(h + 1) * G] = o
         check_parity(host_bits(out16), out32.cpu().numpy(), ref, dtype, "serving loop")
 
