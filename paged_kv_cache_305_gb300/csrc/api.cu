@@ -15,6 +15,12 @@
 #include "pagedattn.h"
 #include "pagedattn_testing.h"
 
+// Share (%) of every row's partitions that the decode kernel hands out at run
+// time (0: the whole split is static).
+#ifndef PA_DECODE_DYNAMIC_PERCENT
+#define PA_DECODE_DYNAMIC_PERCENT pa::kDynamicPercent
+#endif
+
 namespace {
 
 thread_local std::string g_error;
@@ -174,8 +180,8 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, in
   WorkspaceLayout w{};
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
   if (max_partitions <= 1) return w;
-  w.count_off = 0;
-  w.lse_off = round_up(rows * sizeof(int), 256);
+  w.count_off = kWorkspaceHeader;
+  w.lse_off = round_up(kWorkspaceHeader + rows * sizeof(int), 256);
   w.out_off = w.lse_off + round_up(rows * max_partitions * sizeof(float), 256);
   w.total = w.out_off + rows * max_partitions * static_cast<size_t>(head_dim) * sizeof(float);
   return w;
@@ -449,7 +455,8 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
   rc = bad_counter(&bad);
   if (rc != PA_OK) return rc;
   if (wl.total > 0) {
-    const size_t counter_bytes = static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int);
+    const size_t counter_bytes =
+        pa::kWorkspaceHeader + static_cast<size_t>(num_seqs) * num_kv_heads * sizeof(int);
     cudaError_t e = prepare_workspace(workspace, counter_bytes, wl.lse_off, stream);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(workspace counters)");
   }
@@ -480,6 +487,11 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
   a.new_value = new_value;
   char* ws = static_cast<char*>(workspace);
   a.ws_count = wl.total ? reinterpret_cast<int*>(ws + wl.count_off) : nullptr;
+  // the trailing partitions of rows are handed out at run time only with a
+  // workspace (its header holds the claim counter)
+  a.ws_claim = wl.total ? reinterpret_cast<unsigned long long*>(ws) : nullptr;
+  a.ws_done = wl.total ? reinterpret_cast<unsigned*>(ws + 8) : nullptr;
+  a.dyn_percent = wl.total ? PA_DECODE_DYNAMIC_PERCENT : 0;
   a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
   a.ws_out = wl.total ? reinterpret_cast<float*>(ws + wl.out_off) : nullptr;
   a.bad = bad;

@@ -57,6 +57,7 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kTileTokens = 16;  // tokens per warp tile (the k extent of the P.V product)
 constexpr int kRows = 16;        // query-head rows of one tensor-core tile
 constexpr int kIdDepth = 8;      // tiles whose table ids are in flight ahead of their copies
+constexpr int kDynMaxParts = 32;  // rows with more partitions get no dynamic ones
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Seg {
@@ -79,7 +80,7 @@ struct Geometry {
   static constexpr int kSegBytes = kMaxSegments * static_cast<int>(sizeof(Seg));
   static constexpr int kFixedBytes = kPipeBytes + kMLBytes + kSegBytes;
   static constexpr int kOStride = D + 4;  // fp32 row stride of a warp's state in the merge area
-  static_assert(kPipeBytes >= kWarps * 8, "the schedule scan reuses the ring area");
+  static_assert(kPipeBytes >= 2 * kWarps * 8, "the schedule scan reuses the ring area");
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -144,24 +145,53 @@ paged_decode_kernel(const DecodeArgs a) {
 
   auto clamp_len = [&](int L) { return L < 0 ? 0 : (L > Lmax ? Lmax : L); };
   auto nparts_of = [&](int L) { return L > 0 ? (L + Pt - 1) / Pt : 1; };
+  // The trailing d partitions of every row of sequence s are handed out one
+  // by one at run time (claimed through a counter in the workspace) to the
+  // CTAs that finish their static share first; the rest of the row (its
+  // "lead", at least one partition) is split statically. d is a function of
+  // the data alone: about dyn_percent % of the row's partitions, the
+  // fraction rounded up or down by a fixed per-sequence offset.
+  auto dyn_of = [&](int np, int s) -> int {
+    // long rows (more than kDynMaxParts partitions) keep a static split: they
+    // balance well already, and their many pieces would make the merge long
+    if (a.dyn_percent <= 0 || np < 2 || np > kDynMaxParts) return 0;
+    const long long off = (static_cast<unsigned>(s) * 2654435761u) % 100u;
+    const long long d = (static_cast<long long>(np) * a.dyn_percent + off) / 100;
+    return static_cast<int>(min(d, static_cast<long long>(np - 1)));
+  };
+  struct Lead {
+    int L, npl, d;  // length, lead partitions, dynamic partitions
+    long long w;    // weight of the lead: its tokens + kUnitCost per partition
+  };
+  auto lead_of = [&](int s) -> Lead {
+    Lead r;
+    r.L = clamp_len(a.seq_lens[s]);
+    const int np = nparts_of(r.L);
+    r.d = dyn_of(np, s);
+    r.npl = np - r.d;
+    r.w = min(static_cast<long long>(r.L), static_cast<long long>(r.npl) * Pt) +
+          static_cast<long long>(r.npl) * kUnitCost;
+    return r;
+  };
 
   // ======================= schedule ========================================
   // Rows are taken head-group-major: row R = hg * S + s, so the rows of one
   // head group over all sequences are consecutive and sequences that share
   // prefix blocks (consecutive in the batch) re-read them back to back, from
-  // L2. A sequence of length L has ceil(L / Pt) partitions per row (one if L
-  // is 0), each weighing its tokens plus kUnitCost; every CTA computes the
-  // same prefix of these weights over the sequences (one pass, Wseq), and the
-  // positions of head group hg are offset by hg * Wseq. CTA c owns the
+  // L2. The lead of a row of length L has npl partitions (one if L is 0),
+  // each weighing its tokens plus kUnitCost; every CTA computes the same
+  // prefix of these weights over the sequences (one pass, Wseq), and the
+  // positions of head group hg are offset by hg * Wseq. CTA c owns the lead
   // partitions whose start position lies in [first_pos(c), first_pos(c + 1)).
   const int per = (S + kThreads - 1) / kThreads;
   const int s_lo = min(S, tid * per), s_hi = min(S, s_lo + per);
-  long long mine = 0;
+  long long mine = 0, dmine = 0;
   for (int s = s_lo; s < s_hi; ++s) {
     const int raw = a.seq_lens[s];
-    const int L = clamp_len(raw);
-    if (raw != L && cta == 0) atomicAdd(a.bad, 1ull);
-    mine += L + static_cast<long long>(nparts_of(L)) * kUnitCost;
+    const Lead ld = lead_of(s);
+    if (raw != ld.L && cta == 0) atomicAdd(a.bad, 1ull);
+    mine += ld.w;
+    dmine += ld.d;
   }
   long long incl = mine;  // inclusive scan within the warp
 #pragma unroll
@@ -169,8 +199,12 @@ paged_decode_kernel(const DecodeArgs a) {
     const long long v = __shfl_up_sync(kFull, incl, off);
     if (lane >= off) incl += v;
   }
+  long long dsum = dmine;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(kFull, dsum, off);
   long long* sScan = reinterpret_cast<long long*>(sPipe);
   if (lane == 31) sScan[warp] = incl;
+  if (lane == 0) sScan[kWarps + warp] = dsum;
   if (tid == 0) {
     sRange[0] = NG; sRange[1] = 0; sRange[2] = 0;
     sRange[3] = NG; sRange[4] = 0; sRange[5] = 0;
@@ -179,13 +213,17 @@ paged_decode_kernel(const DecodeArgs a) {
   __syncthreads();
   long long base = incl - mine;
   for (int w = 0; w < warp; ++w) base += sScan[w];
-  long long Wseq = 0;
-  for (int w = 0; w < kWarps; ++w) Wseq += sScan[w];
+  long long Wseq = 0, Dseq = 0;
+  for (int w = 0; w < kWarps; ++w) {
+    Wseq += sScan[w];
+    Dseq += sScan[kWarps + w];
+  }
   const long long Wtot = Wseq * NG;
+  const long long Dtot = a.ws_claim != nullptr ? Dseq * NG : 0;  // dynamic partitions
   const long long tau_b = first_pos(cta, C, Wtot);
   const long long tau_e = first_pos(cta + 1, C, Wtot);
-  // the first partition at or after position tau, found by the thread whose
-  // chunk of sequences holds tau's offset within its head group
+  // the first lead partition at or after position tau, found by the thread
+  // whose chunk of sequences holds tau's offset within its head group
   for (int which = 0; which < 2; ++which) {
     const long long tau = which == 0 ? tau_b : tau_e;
     if (tau >= Wtot) continue;  // past the last partition: the default (NG, 0, 0)
@@ -197,16 +235,15 @@ paged_decode_kernel(const DecodeArgs a) {
     int rs = s_hi, rp = 0;
     long long rbase = base + mine;
     for (int s = s_lo; s < s_hi; ++s) {
-      const int L = clamp_len(a.seq_lens[s]);
-      const int np = nparts_of(L);
-      const long long se = sb + L + static_cast<long long>(np) * kUnitCost;
+      const Lead ld = lead_of(s);
+      const long long se = sb + ld.w;
       if (off <= sb) {
         rs = s; rp = 0; rbase = sb;
         break;
       }
       if (off < se) {
         const long long p = (off - sb + UW - 1) / UW;
-        if (p >= np) {
+        if (p >= ld.npl) {
           rs = s + 1; rp = 0; rbase = se;
         } else {
           rs = s; rp = static_cast<int>(p); rbase = sb;
@@ -226,8 +263,25 @@ paged_decode_kernel(const DecodeArgs a) {
   const int pb = sRange[2];
   const long long Re = static_cast<long long>(sRange[3]) * S + sRange[4];
   const int pe = sRange[5];
-  if (Rb == Re && pb == pe) return;  // this CTA owns no partition
-  const long long nseg_total = (Re - Rb) + (pe > 0 ? 1 : 0);
+  const long long nseg_total =
+      (Rb == Re && pb == pe) ? 0 : (Re - Rb) + (pe > 0 ? 1 : 0);  // static segments
+
+  // static lead pieces of the row whose lead starts at position rowbase and
+  // has npl partitions: their number, and the index of the one CTA c0 owns
+  auto lead_pieces = [&](long long rowbase, int npl, int c0, int* me) -> int {
+    int c = owner_of(rowbase, C, Wtot);
+    int k = 0;
+    *me = -1;
+    while (true) {
+      if (c == c0) *me = k;
+      if (c + 1 >= C) break;
+      const long long pn = (first_pos(c + 1, C, Wtot) - rowbase + UW - 1) / UW;
+      if (pn >= npl) break;
+      c = owner_of(rowbase + pn * UW, C, Wtot);
+      ++k;
+    }
+    return k + 1;
+  };
 
   // ======================= per-warp state ===================================
   unsigned char* wpipe = sPipe + warp * STAGES * Geo::kStageBytes;
@@ -274,43 +328,96 @@ paged_decode_kernel(const DecodeArgs a) {
     }
   };
 
-  for (long long b0 = 0; b0 < nseg_total; b0 += kMaxSegments) {
-    const int nseg = static_cast<int>(min(static_cast<long long>(kMaxSegments), nseg_total - b0));
-    // ---- segment records of this batch -------------------------------------
-    if (tid < nseg) {
-      const long long R = Rb + b0 + tid;
-      const int hg = static_cast<int>(R / S), s = static_cast<int>(R % S);
-      const int L = clamp_len(a.seq_lens[s]);
-      const int np = nparts_of(L);
-      const int pf = R == Rb ? pb : 0;
-      const int pl = R == Re ? pe : np;
-      Seg g;
-      g.s = s;
-      g.hg = hg;
-      g.t0 = pf * Pt;
-      g.t1 = static_cast<int>(min(static_cast<long long>(pl) * Pt, static_cast<long long>(L)));
-      g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
-      g.piece = -1;
-      g.npieces = 1;
-      g.L = L;
-      if (!(pf == 0 && pl == np)) {
-        // a row cut between CTAs: walk its owners in order to find this CTA's
-        // piece index and the number of pieces
-        const long long rowbase = R == Rb ? sW[1] : sW[2];
-        int c = owner_of(rowbase, C, Wtot);
-        int k = 0, me = -1;
-        while (true) {
-          if (c == cta) me = k;
-          if (c + 1 >= C) break;
-          const long long pn = (first_pos(c + 1, C, Wtot) - rowbase + UW - 1) / UW;
-          if (pn >= np) break;
-          c = owner_of(rowbase + pn * UW, C, Wtot);
-          ++k;
+  // one dynamic partition: record of the u-th one (warp 0; in head group
+  // u / Dseq, sequences in order, each row's trailing partitions in order)
+  auto locate_unit = [&](unsigned long long u) {
+    const int hg = static_cast<int>(u / static_cast<unsigned long long>(Dseq));
+    const long long off = static_cast<long long>(u) - static_cast<long long>(hg) * Dseq;
+    long long acc_d = 0, acc_w = 0;
+    for (int s0 = 0; s0 < S; s0 += 32) {
+      const int s = s0 + lane;
+      Lead ld{0, 0, 0, 0};
+      if (s < S) ld = lead_of(s);
+      long long id = ld.d, iw = ld.w;  // inclusive scans over the 32 sequences
+#pragma unroll
+      for (int k = 1; k < 32; k <<= 1) {
+        const long long vd = __shfl_up_sync(kFull, id, k);
+        const long long vw = __shfl_up_sync(kFull, iw, k);
+        if (lane >= k) {
+          id += vd;
+          iw += vw;
         }
-        g.piece = me;
-        g.npieces = k + 1;
       }
-      sSeg[tid] = g;
+      const long long td = __shfl_sync(kFull, id, 31), tw = __shfl_sync(kFull, iw, 31);
+      if (off < acc_d + td) {  // warp-uniform
+        const long long lo = acc_d + id - ld.d;
+        if (s < S && lo <= off && off < acc_d + id) {
+          const int i = static_cast<int>(off - lo);
+          int me;
+          const int ns = lead_pieces(static_cast<long long>(hg) * Wseq + acc_w + iw - ld.w, ld.npl,
+                                     -1, &me);
+          Seg g;
+          g.s = s;
+          g.hg = hg;
+          g.t0 = (ld.npl + i) * Pt;
+          g.t1 = static_cast<int>(min(static_cast<long long>(g.t0) + Pt, static_cast<long long>(ld.L)));
+          g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
+          g.piece = ns + i;
+          g.npieces = ns + ld.d;
+          g.L = ld.L;
+          sSeg[0] = g;
+        }
+        return;
+      }
+      acc_d += td;
+      acc_w += tw;
+    }
+  };
+
+  // Batches of segment records: the static segments (kMaxSegments at a time),
+  // then one claimed dynamic partition at a time until none is left.
+  __shared__ unsigned long long sClaim;
+  long long b0 = 0;
+  for (;;) {
+    int nseg;
+    if (b0 < nseg_total) {
+      nseg = static_cast<int>(min(static_cast<long long>(kMaxSegments), nseg_total - b0));
+      // ---- static segment records of this batch ---------------------------------
+      if (tid < nseg) {
+        const long long R = Rb + b0 + tid;
+        const int hg = static_cast<int>(R / S), s = static_cast<int>(R % S);
+        const Lead ld = lead_of(s);
+        const int pf = R == Rb ? pb : 0;
+        const int pl = R == Re ? pe : ld.npl;
+        Seg g;
+        g.s = s;
+        g.hg = hg;
+        g.t0 = pf * Pt;
+        g.t1 = static_cast<int>(min(static_cast<long long>(pl) * Pt, static_cast<long long>(ld.L)));
+        g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
+        g.piece = -1;
+        g.npieces = 1;
+        g.L = ld.L;
+        const bool cut = !(pf == 0 && pl == ld.npl);
+        if (cut || ld.d > 0) {
+          // a row cut between CTAs, or one with dynamic partitions: its lead
+          // pieces in CTA order come first, then one piece per dynamic partition
+          int me = 0, ns = 1;
+          if (cut) ns = lead_pieces(R == Rb ? sW[1] : sW[2], ld.npl, cta, &me);
+          g.piece = me;
+          g.npieces = ns + ld.d;
+        }
+        sSeg[tid] = g;
+      }
+      b0 += nseg;
+    } else {
+      if (Dtot == 0) break;
+      if (tid == 0) sClaim = atomicAdd(a.ws_claim, 1ull);
+      __syncthreads();
+      const unsigned long long u = sClaim;
+      if (u >= static_cast<unsigned long long>(Dtot)) break;  // uniform
+      if (warp == 0) locate_unit(u);
+      nseg = 1;
     }
     __syncthreads();
     load_q(sSeg[0]);
@@ -703,6 +810,14 @@ paged_decode_kernel(const DecodeArgs a) {
     }
     cp_async_wait<0>();
     __syncthreads();  // the segment records are rewritten for the next batch
+  }
+  if (a.ws_claim != nullptr && tid == 0) {
+    // the last CTA to finish (every claim made) leaves the counters at zero
+    __threadfence();
+    if (atomicAdd(a.ws_done, 1u) == static_cast<unsigned>(C - 1)) {
+      atomicExch(a.ws_claim, 0ull);
+      atomicExch(a.ws_done, 0u);
+    }
   }
 }
 

@@ -73,9 +73,9 @@ extern "C" int pa_decode_no_alloc(void* out, const void* query, const void* key_
   if (need > 0 && num_seqs > 0) {
     int rc = scratch_address(&ws);
     if (rc != PA_OK) return rc;
-    // the arrival counters at the start of the scratch must be zero; the
-    // previous call's contents are still there
-    const size_t counters = static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int);
+    // the header and arrival counters at the start of the scratch must be
+    // zero; the previous call's contents are still there
+    const size_t counters = pa::kWorkspaceHeader + static_cast<size_t>(num_seqs) * num_q_heads * sizeof(int);
     cudaError_t e = cudaMemsetAsync(ws, 0, counters, stream);
     if (e != cudaSuccess) {
       char msg[256];

@@ -35,6 +35,9 @@ struct DecodeArgs {
   float* ws_out;       // [S, Hq, max_partitions, d] fp32 partial outputs (normalised)
   float* ws_lse;       // [S, Hq, max_partitions] fp32 base-2 log-sum-exp
   int* ws_count;       // [S * Hkv] arrival counters (zero between calls)
+  unsigned long long* ws_claim;  // dynamic partitions claimed so far (zero between calls), or null
+  unsigned* ws_done;             // CTAs finished (zero between calls)
+  int dyn_percent;     // share (%) of each row's partitions handed out at run time
   unsigned long long* bad;  // device counter of rejected indices
 };
 
@@ -72,9 +75,15 @@ int set_error(int code, const char* msg);
 void clear_error();
 
 // Workspace carve-up shared by pa_decode_workspace_bytes and pa_decode.
+// Layout: a 256-byte header (the dynamic-partition claim counter and the
+// count of finished CTAs), the per-(sequence, kv head) arrival counters, then
+// the fp32 partial results.
 struct WorkspaceLayout {
   size_t count_off, lse_off, out_off, total;
 };
+constexpr size_t kWorkspaceHeader = 256;
+// Percentage of each row's partitions the decode kernel hands out at run time.
+constexpr int kDynamicPercent = 8;
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions);
 
 // Scheduling of the persistent decode kernel: a partition weighs its tokens

@@ -74,14 +74,15 @@ def test_library_is_built_for_sm_103a_only():
 
 
 def test_workspace_bytes_arithmetic(lib):
-    # S * Hq counters, then S * Hq * P lse values, then S * Hq * P * d outputs (fp32)
+    # a 256-byte header (claim counter, finished CTAs), S * Hq counters, then
+    # S * Hq * P lse values, then S * Hq * P * d outputs (fp32)
     def expect(S, Hq, d, MB, B, pt):
         P = -(-(MB * B) // (pt or 512))
         if P <= 1:
             return 0
         r = lambda x: -(-x // 256) * 256
         rows = S * Hq
-        return r(rows * 4) + r(rows * P * 4) + rows * P * d * 4
+        return r(256 + rows * 4) + r(rows * P * 4) + rows * P * d * 4
     for args in [(128, 32, 128, 512, 16, 0), (8, 64, 128, 8192, 16, 512), (4, 4, 64, 8, 16, 0),
                  (3, 6, 64, 40, 1, 16), (256, 32, 128, 24, 64, 64)]:
         assert pa.decode_workspace_bytes(*args) == expect(*args), args

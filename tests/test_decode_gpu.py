@@ -198,9 +198,10 @@ def test_repeatable_and_workspace_reusable():
     a = host_bits(dc.decode()).copy()
     b = host_bits(dc.decode()).copy()
     assert np.array_equal(a, b)
-    # the arrival counters are back at zero after every call
+    # the header (claim counter, finished CTAs) and the arrival counters are
+    # back at zero after every call
     ws = dc.workspace
-    assert int(ws[: case.num_seqs * case.num_q_heads * 4].view(torch.int32).abs().sum()) == 0
+    assert int(ws[: 256 + case.num_seqs * case.num_kv_heads * 4].view(torch.int32).abs().sum()) == 0
     ref = oracle.paged_decode(case.query, case.key_cache, case.value_cache, case.block_tables,
                               case.seq_lens, 16, case.scale, "bf16")
     assert np.array_equal(_parity(dc, ref), a)
