@@ -230,15 +230,14 @@ size_t pa_decode_no_alloc_scratch_bytes(void);
  * Runs on the tcgen05 tensor cores (whole blocks of 8..64 tokens copied by
  * TMA, smaller blocks row by row). num_blocks * block_size must be below 2^31
  * (PA_ERR_UNSUPPORTED otherwise).
- * Arithmetic: q.K in the input type with fp32 accumulation; every softmax
- * weight enters P.V rounded to fp16 (bf16 V is converted to fp16 for that
- * product, exactly inside fp16's range), with fp32 accumulation, and each row's
- * sum of weights adds exactly those rounded weights, so the rounding error of
- * a weight largely cancels between the weighted sum and the sum: the result
- * is off by at most about 2^-11 * max_t |V_t - out| from the weights'
- * rounding. bf16 inputs with a V value beyond fp16's range (+-65504): the
- * query tiles that meet one are computed again with bf16 weights split into
- * a head and the rounding of the remainder (relative error below 2^-16).
+ * Arithmetic: q.K in the input type with fp32 accumulation. fp16: every
+ * softmax weight enters P.V rounded to fp16, in one product with fp32
+ * accumulation, and each row's sum of weights adds exactly those rounded
+ * weights, so a weight's rounding error largely cancels between the weighted
+ * sum and the sum (the result is off by at most about 2^-11 * max_t |V_t -
+ * out| from that rounding). bf16: every weight enters as the sum of two bf16
+ * parts (its upper half and the rounding of the remainder, relative error
+ * below 2^-16), two products.
  */
 int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,

@@ -15,10 +15,11 @@
 //              the causal limit (only in warps holding a diagonal tile: a
 //              warp-uniform branch, so other tiles carry no per-element
 //              selects), keeps the running max / sum (base 2), writes the
-//              weights into tensor memory as a 16-bit head plus the 16-bit
-//              rounding of the remainder, and rescales its output row when the
-//              max has grown by more than 2^8 since the last rescale; finally
-//              divides by the sum and stores the row.
+//              weights into tensor memory (fp16 inputs: rounded to fp16, and
+//              the sum adds those rounded weights; bf16: a 16-bit head plus
+//              the 16-bit rounding of the remainder), and rescales its output
+//              row when the max has grown by more than 2^8 since the last
+//              rescale; finally divides by the sum and stores the row.
 //   warps 4, 5 producers of the K and the V tiles (each on its own, so K
 //              runs ahead of V): whole blocks of 8+ tokens by TMA (one box
 //              per block, the whole head dim, straight from the block
@@ -28,7 +29,8 @@
 //   warp 6     one thread issues the products: S_{j+1} = Q K_{j+1}^T (smem x
 //              smem, M=128, N=64) as soon as the softmax has read S_j, and
 //              O += P_j V_j (weights from tensor memory, V from smem read
-//              MN-major, N = head dim) for the head and the remainder.
+//              MN-major, N = head dim): one product for fp16, the head and
+//              the remainder for bf16.
 // Tensor memory (256 columns): S at 0, P at 64, O at 128, so the product of
 // the next S overlaps the whole softmax of the current tile. All waits are
 // bounded; a wait that gives up is counted and the CTA winds down.
@@ -60,7 +62,9 @@ constexpr uint32_t kColS = 0;    // S, 64 fp32 columns
 constexpr uint32_t kColP = 64;   // P: 32 columns of packed 16-bit heads, 32 of remainders
 constexpr uint32_t kColO = 128;  // O, head_dim fp32 columns
 constexpr float kRescaleLog2 = 8.f;
-constexpr float kWeightLog2Offset = 6.f;  // fp16 weights carry a factor 2^6
+// fp16 inputs: the weights carry a factor 2^6 (at most 2^14 under the lazy
+// rescale), so weights down to 2^-20 of the reference max stay normal fp16
+constexpr float kWeightLog2Offset = 6.f;
 constexpr unsigned kFull = 0xffffffffu;
 
 template <int D>
@@ -151,38 +155,6 @@ __device__ __forceinline__ float add_f16x2(float acc, uint32_t h) {
       : "+f"(acc)
       : "r"(h));
   return acc;
-}
-
-// Two bf16 values to fp16, round to nearest even (exact inside fp16's normal
-// range; beyond +-65504 the result is inf).
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
-  return F16::pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-// A bf16 V tile (kKeys tokens x D) in shared memory converted to fp16 in
-// place, element by element (the layout is unchanged); thread t of the 128
-// softmax threads takes the 16-byte chunks t, t + 128, ...; loads first.
-template <int D>
-__device__ __forceinline__ void convert_v_tile(uint32_t tile, int t) {
-  constexpr int kPer = kKeys * D * 2 / 16 / 128;  // chunks per thread
-  uint4 v[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) v[k] = ld_shared_v4(tile + 16u * static_cast<uint32_t>(t + 128 * k));
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const uint4 w = make_uint4(bf16x2_to_f16x2(v[k].x), bf16x2_to_f16x2(v[k].y),
-                               bf16x2_to_f16x2(v[k].z), bf16x2_to_f16x2(v[k].w));
-    st_shared_v4(tile + 16u * static_cast<uint32_t>(t + 128 * k), w);
-  }
 }
 
 // Bounded wait made uniform across the warp: every lane of a warp that
@@ -291,229 +263,170 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int qp = row_valid ? L - Q + j0 + r / G : last_pos;  // causal limit
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     const float sl2 = fabsf(a.scale_log2);  // the query tile carries the sign
-    for (int pass = 0;; ++pass) {
-      const int base = pass * ntiles;  // tiles of earlier passes (barrier phases run on)
-      // the first pass multiplies fp16 weights with fp16 V (one product per
-      // tile); a bf16 second pass, only after a non-finite result, uses bf16
-      // weights as a head plus the rounding of the remainder (two products)
-      const bool fp16w = !Ty::kIsBf16 || pass == 0;
-      // fp16 weights carry a factor 2^6 (at most 2^14 under the lazy rescale),
-      // so weights down to 2^-20 of the reference max stay normal numbers
-      const float woff = fp16w ? kWeightLog2Offset : 0.f;
-      float m = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of weights
-      for (int j = 0; j < ntiles; ++j) {
-        const int jg = base + j;
-        ok = warp_wait(bar(kBarSFull + (jg & 1)), (jg >> 1) & 1);
+    float m = -INFINITY, l = 0.f;  // running max (base-2 units) and sum of weights
+    for (int j = 0; j < ntiles; ++j) {
+      ok = warp_wait(bar(kBarSFull + (j & 1)), (j >> 1) & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      float sv[kKeys];
+      {
+        uint32_t x0[16], x1[16], x2[16], x3[16];
+        tc::tmem_ld16(lane_addr + kColS, x0);
+        tc::tmem_ld16(lane_addr + kColS + 16, x1);
+        tc::tmem_ld16(lane_addr + kColS + 32, x2);
+        tc::tmem_ld16(lane_addr + kColS + 48, x3);
+        tc::tmem_ld_wait16(x0);
+        tc::tmem_ld_wait16(x1);
+        tc::tmem_ld_wait16(x2);
+        tc::tmem_ld_wait16(x3);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          sv[i] = __uint_as_float(x0[i]);
+          sv[16 + i] = __uint_as_float(x1[i]);
+          sv[32 + i] = __uint_as_float(x2[i]);
+          sv[48 + i] = __uint_as_float(x3[i]);
+        }
+      }
+      // S_j is in registers: S_{j+1} may now be written into the same columns
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kBarSFree));
+      // tokens kb + c with c > lim are past this row's causal limit; a warp
+      // with any such row takes the masked path, the others carry no
+      // per-element selects (warp-uniform branch)
+      const int lim = qp - j * kKeys;
+      const bool diag = __any_sync(kFull, lim < kKeys - 1);
+      bool rescale = false;
+      float alpha = 1.f;
+      uint32_t ph[32], pl[32];
+      auto weights = [&](auto masked) {
+        constexpr bool kMasked = decltype(masked)::value;
+        if constexpr (kMasked) {
+#pragma unroll
+          for (int c = 0; c < kKeys; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
+        }
+        // row max of the raw scores: four chains of three-input maxima
+        float mx4[4];
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float* v = sv + 16 * q4;
+          float mq = max3(v[0], v[1], v[2]);
+#pragma unroll
+          for (int c = 3; c < 15; c += 2) mq = max3(mq, v[c], v[c + 1]);
+          mx4[q4] = fmaxf(mq, v[15]);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
+        rescale = __any_sync(kFull, mn > m + kRescaleLog2);
+        if (rescale) {
+          alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
+          l *= alpha;
+          m = mn;
+        }
+        // weights 2^(s*sl2 - m), the exponent arguments by paired fp32
+        // multiply-adds. fp16 inputs: the fp16 rounding of each weight
+        // (scaled by 2^6), one product with fp16 V, and the row sum adds
+        // exactly those rounded weights, so a weight's rounding error cancels
+        // between the weighted sum and the sum. bf16 inputs: a 16-bit head
+        // (the upper half of the fp32 weight, taken by byte selection) and
+        // the 16-bit rounding of the remainder, two products (the operands of
+        // one product share a type, and V is bf16).
+        constexpr float kOff = Ty::kIsBf16 ? 0.f : kWeightLog2Offset;
+        const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(kOff - m, kOff - m);
+        float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 2 * i;
+          float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
+          if constexpr (kMasked) {  // exact zeros past the limit (also for a zero scale)
+            arg.x = c > lim ? -INFINITY : arg.x;
+            arg.y = c + 1 > lim ? -INFINITY : arg.y;
+          }
+          const float p0 = ex2(arg.x), p1 = ex2(arg.y);
+          if constexpr (Ty::kIsBf16) {
+            rs[i & 3] += p0;
+            rs[i & 3] += p1;
+            const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+            ph[i] = __byte_perm(b0, b1, 0x7632);
+            pl[i] = Ty::pack(p0 - __uint_as_float(b0 & 0xffff0000u),
+                             p1 - __uint_as_float(b1 & 0xffff0000u));
+          } else {
+            ph[i] = Ty::pack(p0, p1);
+            rs[i & 3] = add_f16x2(rs[i & 3], ph[i]);
+          }
+        }
+        l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      };
+      if (diag)
+        weights(std::true_type{});
+      else
+        weights(std::false_type{});
+      if (j > 0) {
+        // P_{j-1} V must be done before P_j overwrites its columns and O is rescaled
+        ok = warp_wait(bar(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1);
         if (!ok) break;
         tc::tc_fence_after();
-        float sv[kKeys];
-        {
-          uint32_t x0[16], x1[16], x2[16], x3[16];
-          tc::tmem_ld16(lane_addr + kColS, x0);
-          tc::tmem_ld16(lane_addr + kColS + 16, x1);
-          tc::tmem_ld16(lane_addr + kColS + 32, x2);
-          tc::tmem_ld16(lane_addr + kColS + 48, x3);
-          tc::tmem_ld_wait16(x0);
-          tc::tmem_ld_wait16(x1);
-          tc::tmem_ld_wait16(x2);
-          tc::tmem_ld_wait16(x3);
+        if (rescale) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            sv[i] = __uint_as_float(x0[i]);
-            sv[16 + i] = __uint_as_float(x1[i]);
-            sv[32 + i] = __uint_as_float(x2[i]);
-            sv[48 + i] = __uint_as_float(x3[i]);
-          }
-        }
-        // S_j is in registers: S_{j+1} may now be written into the same columns
-        tc::tc_fence_before();
-        tc::mbar_arrive(bar(kBarSFree));
-        // tokens kb + c with c > lim are past this row's causal limit; a warp
-        // with any such row takes the masked path, the others carry no
-        // per-element selects (warp-uniform branch)
-        const int lim = qp - j * kKeys;
-        const bool diag = __any_sync(kFull, lim < kKeys - 1);
-        bool rescale = false;
-        float alpha = 1.f;
-        uint32_t ph[32], pl[32];
-        auto weights = [&](auto masked, auto single) {
-          constexpr bool kMasked = decltype(masked)::value;
-          constexpr bool kSingle = decltype(single)::value;
-          if constexpr (kMasked) {
+          for (int c = 0; c < D / 16; ++c) {
+            uint32_t x[16];
+            tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
+            tc::tmem_ld_wait16(x);
 #pragma unroll
-            for (int c = 0; c < kKeys; ++c) sv[c] = c > lim ? -INFINITY : sv[c];
-          }
-          // row max of the raw scores: four chains of three-input maxima
-          float mx4[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const float* v = sv + 16 * q4;
-            float mq = max3(v[0], v[1], v[2]);
-#pragma unroll
-            for (int c = 3; c < 15; c += 2) mq = max3(mq, v[c], v[c + 1]);
-            mx4[q4] = fmaxf(mq, v[15]);
-          }
-          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-          const float mn = fmaxf(m, mx == -INFINITY ? -INFINITY : mx * sl2);
-          rescale = __any_sync(kFull, mn > m + kRescaleLog2);
-          if (rescale) {
-            alpha = ex2(m - mn);  // 0 on the first tile (m = -inf)
-            l *= alpha;
-            m = mn;
-          }
-          // weights 2^(s*sl2 - m + woff), the exponent arguments by paired fp32
-          // multiply-adds. Single product: the fp16 rounding of each weight,
-          // and the row sum adds exactly those rounded weights (so a weight's
-          // rounding error cancels between the numerator and the sum).
-          // Otherwise a 16-bit head and the 16-bit rounding of the remainder
-          // (bf16: the head is the upper half of the fp32 weight, taken by
-          // byte selection; fp16: rounded).
-          const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(woff - m, woff - m);
-          float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 2 * i;
-            float2 arg = f2_split(f2_fma(f2(sv[c], sv[c + 1]), sl2x2, nmx2));
-            if constexpr (kMasked) {  // exact zeros past the limit (also for a zero scale)
-              arg.x = c > lim ? -INFINITY : arg.x;
-              arg.y = c + 1 > lim ? -INFINITY : arg.y;
-            }
-            const float p0 = ex2(arg.x), p1 = ex2(arg.y);
-            if constexpr (kSingle) {
-              ph[i] = F16::pack(p0, p1);
-              rs[i & 3] = add_f16x2(rs[i & 3], ph[i]);
-            } else {
-              rs[i & 3] += p0;
-              rs[i & 3] += p1;
-              if constexpr (Ty::kIsBf16) {
-                const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-                ph[i] = __byte_perm(b0, b1, 0x7632);
-                pl[i] = Ty::pack(p0 - __uint_as_float(b0 & 0xffff0000u),
-                                 p1 - __uint_as_float(b1 & 0xffff0000u));
-              } else {
-                ph[i] = Ty::pack(p0, p1);
-                const float2 d = Ty::unpack(ph[i]);
-                pl[i] = Ty::pack(p0 - d.x, p1 - d.y);
-              }
-            }
-          }
-          l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
-        };
-        if (fp16w) {
-          if (diag)
-            weights(std::true_type{}, std::true_type{});
-          else
-            weights(std::false_type{}, std::true_type{});
-        } else if constexpr (Ty::kIsBf16) {
-          if (diag)
-            weights(std::true_type{}, std::false_type{});
-          else
-            weights(std::false_type{}, std::false_type{});
-        }
-        if constexpr (Ty::kIsBf16) {
-          if (fp16w) {
-            // V_j to fp16, in place, for the single product (the two operands
-            // of one product have one type); a value beyond fp16's range
-            // becomes inf and shows up in the end-of-pass check
-            ok = warp_wait(bar(kBarVFull + (jg & 1)), (jg >> 1) & 1);
-            if (!ok) break;
-            convert_v_tile<D>(sV(jg & 1), tid);
-            tc::fence_async_smem();
-          }
-        }
-        if (j > 0) {
-          // P_{j-1} V must be done before P_j overwrites its columns and O is rescaled
-          ok = warp_wait(bar(kBarODone + ((jg - 1) & 1)), ((jg - 1) >> 1) & 1);
-          if (!ok) break;
-          tc::tc_fence_after();
-          if (rescale) {
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-              uint32_t x[16];
-              tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
-              tc::tmem_ld_wait16(x);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
-              tc::tmem_st16(lane_addr + kColO + 16 * c, x);
-            }
-          }
-        }
-        {
-          uint32_t w[16];
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) w[i] = ph[16 * hh + i];
-            tc::tmem_st16(lane_addr + kColP + 16 * hh, w);  // weights (head part)
-            if (!fp16w) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) w[i] = pl[16 * hh + i];
-              tc::tmem_st16(lane_addr + kColP + 32 + 16 * hh, w);  // weights, remainder
-            }
-          }
-        }
-        tc::tmem_st_wait();
-        tc::tc_fence_before();
-        tc::mbar_arrive(bar(kBarPFull));
-      }
-      const int jl = base + ntiles - 1;  // the pass's last tile
-      if (ok) ok = warp_wait(bar(kBarODone + (jl & 1)), (jl >> 1) & 1);
-      if constexpr (Ty::kIsBf16) {
-        if (pass == 0) {
-          // a V value beyond fp16's range (inf after the conversion) leaves a
-          // non-finite output: then the CTA computes its tile again with bf16
-          // weights and the original bf16 V (inputs that are themselves
-          // non-finite take the second pass too and give the same result)
-          bool nonfinite = false;
-          if (ok) {
-            tc::tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-              uint32_t x[16];
-              tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
-              tc::tmem_ld_wait16(x);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) nonfinite |= !(fabsf(__uint_as_float(x[i])) < INFINITY);
-            }
-          }
-          const bool redo = __syncthreads_or(nonfinite) != 0;
-          const bool failed = __syncthreads_or(!ok) != 0;
-          if (redo && !failed) continue;
-        }
-      }
-      if (ok) {
-        tc::tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        const size_t row = static_cast<size_t>(q0 + j0 + r / G) * a.num_q_heads +
-                           static_cast<size_t>(h) * G + r % G;
-#pragma unroll
-        for (int c = 0; c < D / 16; ++c) {
-          uint32_t x[16];
-          tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
-          tc::tmem_ld_wait16(x);
-          if (!row_valid) continue;
-          if (a.out_f32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              o[i] = make_float4(__uint_as_float(x[4 * i]) * inv, __uint_as_float(x[4 * i + 1]) * inv,
-                                 __uint_as_float(x[4 * i + 2]) * inv,
-                                 __uint_as_float(x[4 * i + 3]) * inv);
-          } else {
-            uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D + 16 * c);
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-              uint4 w;
-              w.x = Ty::pack(__uint_as_float(x[8 * i]) * inv, __uint_as_float(x[8 * i + 1]) * inv);
-              w.y = Ty::pack(__uint_as_float(x[8 * i + 2]) * inv, __uint_as_float(x[8 * i + 3]) * inv);
-              w.z = Ty::pack(__uint_as_float(x[8 * i + 4]) * inv, __uint_as_float(x[8 * i + 5]) * inv);
-              w.w = Ty::pack(__uint_as_float(x[8 * i + 6]) * inv, __uint_as_float(x[8 * i + 7]) * inv);
-              o[i] = w;
-            }
+            for (int i = 0; i < 16; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
+            tc::tmem_st16(lane_addr + kColO + 16 * c, x);
           }
         }
       }
-      break;
+      {
+        uint32_t w[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = ph[16 * hh + i];
+          tc::tmem_st16(lane_addr + kColP + 16 * hh, w);  // weights (bf16: head part)
+          if constexpr (Ty::kIsBf16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = pl[16 * hh + i];
+            tc::tmem_st16(lane_addr + kColP + 32 + 16 * hh, w);  // weights, remainder
+          }
+        }
+      }
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(bar(kBarPFull));
+    }
+    if (ok) ok = warp_wait(bar(kBarODone + ((ntiles - 1) & 1)), ((ntiles - 1) >> 1) & 1);
+    if (ok) {
+      tc::tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const size_t row = static_cast<size_t>(q0 + j0 + r / G) * a.num_q_heads +
+                         static_cast<size_t>(h) * G + r % G;
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        uint32_t x[16];
+        tc::tmem_ld16(lane_addr + kColO + 16 * c, x);
+        tc::tmem_ld_wait16(x);
+        if (!row_valid) continue;
+        if (a.out_f32) {
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.out) + row * D + 16 * c);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            o[i] = make_float4(__uint_as_float(x[4 * i]) * inv, __uint_as_float(x[4 * i + 1]) * inv,
+                               __uint_as_float(x[4 * i + 2]) * inv,
+                               __uint_as_float(x[4 * i + 3]) * inv);
+        } else {
+          uint4* o = reinterpret_cast<uint4*>(static_cast<T*>(a.out) + row * D + 16 * c);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            uint4 w;
+            w.x = Ty::pack(__uint_as_float(x[8 * i]) * inv, __uint_as_float(x[8 * i + 1]) * inv);
+            w.y = Ty::pack(__uint_as_float(x[8 * i + 2]) * inv, __uint_as_float(x[8 * i + 3]) * inv);
+            w.z = Ty::pack(__uint_as_float(x[8 * i + 4]) * inv, __uint_as_float(x[8 * i + 5]) * inv);
+            w.w = Ty::pack(__uint_as_float(x[8 * i + 6]) * inv, __uint_as_float(x[8 * i + 7]) * inv);
+            o[i] = w;
+          }
+        }
+      }
     }
   } else if (warp == kKWarp || warp == kVWarp) {
     // ---------------- producers: K (or V) tiles of 64 tokens through the block table
@@ -527,7 +440,6 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     const int nb = kKeys >> shift;  // blocks per tile (1..8)
     const int32_t* trow = a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq;
     const size_t slot_stride = static_cast<size_t>(a.num_kv_heads) * D;
-    bool count_bad = true;  // rejected ids are counted in the first pass only
     // lane i < nb describes block i of a tile: its id (-1: none / out of
     // range) and how many of its B tokens lie before L
     auto block_of = [&](int jt, int& id, int& valid) {
@@ -539,7 +451,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         if (valid > 0) {
           id = __ldg(trow + blk);
           if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-            if (!is_v && count_bad) atomicAdd(a.bad, 1ull);  // counted once, by the K producer
+            if (!is_v) atomicAdd(a.bad, 1ull);  // counted once, by the K producer
             id = -1;
           }
         }
@@ -587,101 +499,85 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         tc::tma_load_5d(dst0 + static_cast<uint32_t>(lane * B * D * 2), map, full_bar, 0, 0, 0,
                         id << (shift - 3), h);
     };
-    // blocks under 8 tokens: lane l holds the cache slots of rows l and l + 32
-    // of a tile (-1: past L or a rejected block id); slots stay below 2^31
-    auto row_slots = [&](int jt, int (&sr)[2]) {
+    if (B < 8) {
+      // Blocks smaller than a swizzle atom: every row by a 16-byte cp.async
+      // (zero fill past L and for rejected ids), two rows per warp
+      // instruction. Each lane then arrives on the tile's barrier when its
+      // copies have landed (cp.async.mbarrier.arrive.noinc, 32 arrivals per
+      // tile); the product thread makes them visible to the tensor cores
+      // (fence.proxy.async) after its wait.
+      constexpr int kCopies = kKeys * kChunks / 32;  // per lane per tile
+      // lane l holds the block ids of rows l and l + 32 of a tile (-1: none)
+      // lane l holds the cache slots of rows l and l + 32 of a tile (-1:
+      // past L or a rejected block id); slots stay below 2^31
+      auto row_slots = [&](int jt, int (&sr)[2]) {
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = jt * kKeys + lane + 32 * u;
-        sr[u] = -1;
-        if (jt < ntiles && t < L) {
-          const int id = __ldg(trow + (t >> shift));
-          if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
-            sr[u] = (id << shift) + (t & (B - 1));
-          else if (!is_v && count_bad && (t & (B - 1)) == 0)
-            atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
-        }
-      }
-    };
-    for (int pass = 0;; ++pass) {
-      const int base = pass * ntiles;  // tiles of earlier passes (barrier phases run on)
-      count_bad = pass == 0;
-      if (B < 8) {
-        // Blocks smaller than a swizzle atom: every row by a 16-byte cp.async
-        // (zero fill past L and for rejected ids), two rows per warp
-        // instruction. Each lane then arrives on the tile's barrier when its
-        // copies have landed (cp.async.mbarrier.arrive.noinc, 32 arrivals per
-        // tile); the product thread makes them visible to the tensor cores
-        // (fence.proxy.async) after its wait.
-        constexpr int kCopies = kKeys * kChunks / 32;  // per lane per tile
-        // this lane's 16-byte chunk of a row: c = lane % kChunks, rows
-        // kLaneRows * k + lane / kChunks
-        constexpr int kLaneRows = 32 / kChunks;
-        const int c = lane % kChunks, r0 = lane / kChunks;
-        const T* cbase = cache + static_cast<size_t>(h) * D + c * 8;
-        int sn[2];
-        row_slots(0, sn);
-        int j = 0;
-        for (; j < ntiles; ++j) {
-          const int jg = base + j;
-          const int st = jg & 1;
-          const int sr[2] = {sn[0], sn[1]};
-          row_slots(j + 1, sn);  // next tile's table entries, ahead of time
-          if (jg >= kStages) {
-            ok = warp_wait(bar(empty0 + st), ((jg >> 1) - 1) & 1);
-            if (!ok) break;
+        for (int u = 0; u < 2; ++u) {
+          const int t = jt * kKeys + lane + 32 * u;
+          sr[u] = -1;
+          if (jt < ntiles && t < L) {
+            const int id = __ldg(trow + (t >> shift));
+            if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+              sr[u] = (id << shift) + (t & (B - 1));
+            else if (!is_v && (t & (B - 1)) == 0)
+              atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
           }
-          const uint32_t dst0 = is_v ? sV(st) : sK(st);
+        }
+      };
+      // this lane's 16-byte chunk of a row: c = lane % kChunks, rows
+      // kLaneRows * k + lane / kChunks
+      constexpr int kLaneRows = 32 / kChunks;
+      const int c = lane % kChunks, r0 = lane / kChunks;
+      const T* cbase = cache + static_cast<size_t>(h) * D + c * 8;
+      int sn[2];
+      row_slots(0, sn);
+      int j = 0;
+      for (; j < ntiles; ++j) {
+        const int st = j & 1;
+        const int sr[2] = {sn[0], sn[1]};
+        row_slots(j + 1, sn);  // next tile's table entries, ahead of time
+        if (j >= kStages) {
+          ok = warp_wait(bar(empty0 + st), ((j >> 1) - 1) & 1);
+          if (!ok) break;
+        }
+        const uint32_t dst0 = is_v ? sV(st) : sK(st);
 #pragma unroll
-          for (int k = 0; k < kCopies; ++k) {
-            const int row = kLaneRows * k + r0;
-            // every lane of this copy reads rows in the same half of the tile
-            const int slot = __shfl_sync(kFull, sr[(kLaneRows * k) >> 5], row & 31);
-            const bool okr = slot >= 0;
-            cp_async_16(dst0 + kv_off<D>(row, c),
-                        cbase + static_cast<size_t>(okr ? slot : 0) * slot_stride, okr);
-          }
-          tc::cp_async_mbar_arrive_noinc(bar(full0 + st));
+        for (int k = 0; k < kCopies; ++k) {
+          const int row = kLaneRows * k + r0;
+          // every lane of this copy reads rows in the same half of the tile
+          const int slot = __shfl_sync(kFull, sr[(kLaneRows * k) >> 5], row & 31);
+          const bool okr = slot >= 0;
+          cp_async_16(dst0 + kv_off<D>(row, c),
+                      cbase + static_cast<size_t>(okr ? slot : 0) * slot_stride, okr);
         }
-        // copies still in flight (only after a wait gave up) land before exit
-        for (int jj = base + max(0, j - kStages); jj < base + j; ++jj)
-          tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
-      } else {
-        int id_n, valid_n;
-        block_of(0, id_n, valid_n);
-        int j = 0;
-        for (; j < ntiles; ++j) {
-          const int jg = base + j;
-          const int st = jg & 1;
-          const int id = id_n, valid = valid_n;
-          block_of(j + 1, id_n, valid_n);  // next tile's table entries, ahead of time
-          const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
-          if (jg >= kStages) {
-            ok = warp_wait(bar(empty0 + st), ((jg >> 1) - 1) & 1);
-            if (!ok) break;
-          }
-          fill(cache, map, is_v ? sV(st) : sK(st), bar(full0 + st), id, valid, whole);
-        }
-        // copies still in flight (only after a wait gave up) must land before exit
-        for (int jj = base + max(0, j - kStages); jj < base + j; ++jj)
-          tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
+        tc::cp_async_mbar_arrive_noinc(bar(full0 + st));
       }
-      if constexpr (Ty::kIsBf16) {
-        if (pass == 0) {  // the softmax warps decide whether a bf16 pass follows
-          const bool redo = __syncthreads_or(0) != 0;
-          const bool failed = __syncthreads_or(!ok) != 0;
-          if (redo && !failed) continue;
-        }
+      // copies still in flight (only after a wait gave up) land before exit
+      for (int jj = max(0, j - kStages); jj < j; ++jj)
+        tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
+    } else {
+    int id_n, valid_n;
+    block_of(0, id_n, valid_n);
+    int j = 0;
+    for (; j < ntiles; ++j) {
+      const int st = j & 1;
+      const int id = id_n, valid = valid_n;
+      block_of(j + 1, id_n, valid_n);  // next tile's table entries, ahead of time
+      const unsigned whole = __ballot_sync(kFull, lane < nb && id >= 0 && valid == B);
+      if (j >= kStages) {
+        ok = warp_wait(bar(empty0 + st), ((j >> 1) - 1) & 1);
+        if (!ok) break;
       }
-      break;
+      fill(cache, map, is_v ? sV(st) : sK(st), bar(full0 + st), id, valid, whole);
     }
-  } else if (warp == kMmaWarp) {
+    // copies still in flight (only after a wait gave up) must land before exit
+    for (int jj = max(0, j - kStages); jj < j; ++jj)
+      tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
+    }
+  } else if (warp == kMmaWarp && lane == 0) {
     // ---------------- products, one thread; descriptors built once, moved by
     // adding (byte offset >> 4) to the start-address field
     const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
-    // P V: fp16 weights with fp16 V (single product), or the input type for
-    // both (bf16 second pass: head and remainder)
-    const uint32_t id_o16 = tc::idesc_f16(kRows, D, false, true);
     const uint32_t id_o = tc::idesc_f16(kRows, D, Ty::kIsBf16, true);
     const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
     // K read K-major: 8-token groups kGroupBytes apart (SBO)
@@ -694,8 +590,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     auto kstep = [](int ks) {  // K-major: slice ks / 4, 32 bytes per 16 elements
       return static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
     };
-    auto issue_s = [&](int jg) {
-      const int st = jg & 1;
+    auto issue_s = [&](int j) {
+      const int st = j & 1;
       const uint32_t d = tmem + kColS;
       const uint64_t dk = dk0 + st * kStageStep;
 #pragma unroll
@@ -706,73 +602,50 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       tc::tc_commit(bar(kBarSFull + st));
     };
     uint32_t last_bar = 0, last_parity = 0;  // the latest commit
-    for (int pass = 0;; ++pass) {
-      if (lane == 0) {
-        const int base = pass * ntiles;
-        const bool fp16w = !Ty::kIsBf16 || pass == 0;
-        // a stalled test launch first waits on a barrier that nothing signals:
-        // the wait runs out, no product is issued, and every warp winds down
-        if (pass == 0 && a.stall_for_test) ok = tc::mbar_wait(bar(kBarNever), 0);
-        ok = ok && (pass > 0 || tc::mbar_wait(bar(kBarQFull), 0)) &&
-             tc::mbar_wait(bar(kBarKFull + (base & 1)), (base >> 1) & 1);
-        if (ok) {
-          tc::tc_fence_after();
-          if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products
-          issue_s(base);
-          last_bar = bar(kBarSFull + (base & 1));
-          last_parity = (base >> 1) & 1;
-        }
-        for (int j = 0; j < ntiles && ok; ++j) {
-          const int jg = base + j;
-          const int b = jg & 1;
-          if (j + 1 < ntiles) {
-            // S_{j+1} overwrites S_j: wait until the softmax has read it
-            ok = tc::mbar_wait(bar(kBarSFree), jg & 1) &&
-                 tc::mbar_wait(bar(kBarKFull + ((jg + 1) & 1)), ((jg + 1) >> 1) & 1);
-            if (!ok) break;
-            tc::tc_fence_after();
-            if (row_copies) tc::fence_async_smem();
-            issue_s(jg + 1);
-            last_bar = bar(kBarSFull + ((jg + 1) & 1));
-            last_parity = ((jg + 1) >> 1) & 1;
-          }
-          ok = tc::mbar_wait(bar(kBarPFull), jg & 1) && tc::mbar_wait(bar(kBarVFull + b), (jg >> 1) & 1);
-          if (!ok) break;
-          tc::tc_fence_after();
-          if (row_copies) tc::fence_async_smem();
-          const uint32_t colP = tmem + kColP;
-          const uint64_t dv = dv0 + b * kStageStep;
-          if (fp16w) {
-#pragma unroll
-            for (int ks = 0; ks < kKeys / 16; ++ks)
-              tc::mma_ts(tmem + kColO, colP + ks * 8, dv + ks * kVStep, id_o16,
-                         (j > 0 || ks > 0) ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int part = 0; part < 2; ++part) {  // weights: head part, then remainder
-#pragma unroll
-              for (int ks = 0; ks < kKeys / 16; ++ks)
-                tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
-                           id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-            }
-          }
-          tc::tc_commit(bar(kBarODone + b));
-          last_bar = bar(kBarODone + b);
-          last_parity = (jg >> 1) & 1;
-        }
-        // nothing this thread issued may still be running at the end of a pass
-        if (last_bar != 0) tc::mbar_wait(last_bar, last_parity);
-      }
-      __syncwarp();
-      if constexpr (Ty::kIsBf16) {
-        if (pass == 0) {  // the softmax warps decide whether a bf16 pass follows
-          const bool redo = __syncthreads_or(0) != 0;
-          const bool failed = __syncthreads_or(!ok) != 0;
-          if (redo && !failed) continue;
-        }
-      }
-      break;
+    // a stalled test launch first waits on a barrier that nothing signals:
+    // the wait runs out, no product is issued, and every warp winds down
+    if (a.stall_for_test) ok = tc::mbar_wait(bar(kBarNever), 0);
+    ok = ok && tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
+    if (ok) {
+      tc::tc_fence_after();
+      if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products
+      issue_s(0);
+      last_bar = bar(kBarSFull);
+      last_parity = 0;
     }
+    for (int j = 0; j < ntiles && ok; ++j) {
+      const int b = j & 1;
+      if (j + 1 < ntiles) {
+        // S_{j+1} overwrites S_j: wait until the softmax has read it
+        ok = tc::mbar_wait(bar(kBarSFree), j & 1) &&
+             tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+        if (!ok) break;
+        tc::tc_fence_after();
+        if (row_copies) tc::fence_async_smem();
+        issue_s(j + 1);
+        last_bar = bar(kBarSFull + ((j + 1) & 1));
+        last_parity = ((j + 1) >> 1) & 1;
+      }
+      ok = tc::mbar_wait(bar(kBarPFull), j & 1) && tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
+      if (!ok) break;
+      tc::tc_fence_after();
+      if (row_copies) tc::fence_async_smem();
+      const uint32_t colP = tmem + kColP;
+      const uint64_t dv = dv0 + b * kStageStep;
+      // fp16: one product; bf16: the weights' head part, then the remainder
+#pragma unroll
+      for (int part = 0; part < (Ty::kIsBf16 ? 2 : 1); ++part) {
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 16; ++ks)
+          tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
+                     id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+      }
+      tc::tc_commit(bar(kBarODone + b));
+      last_bar = bar(kBarODone + b);
+      last_parity = (j >> 1) & 1;
+    }
+    // nothing this thread issued may still be running when the CTA ends
+    if (last_bar != 0) tc::mbar_wait(last_bar, last_parity);
   }
 
   if (!ok && lane == 0) atomicAdd(a.timeouts, 1ull);
