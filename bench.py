@@ -712,7 +712,8 @@ def _bf16_peak():
     return 1900.0, "fallback bf16 burst"
 
 
-def measure_prefill(ctx, chunk, B, tname, steps, warmup, S=16, Hq=32, Hkv=8, d=128):
+def measure_prefill(ctx, chunk, B, tname, steps, warmup, S=16, Hq=32, Hkv=8, d=128,
+                    workspace=True):
     """Paged causal prefill of S sequences (Hq/Hkv heads, head_dim d, block size
     B): a chunk of `chunk` new tokens per sequence whose K/V are in the cache
     after ctx - chunk older tokens (ctx = chunk: whole prompts). Returns
@@ -730,17 +731,25 @@ def measure_prefill(ctx, chunk, B, tname, steps, warmup, S=16, Hq=32, Hkv=8, d=1
     starts = torch.arange(0, (S + 1) * chunk, chunk, dtype=torch.int32).cuda()
     q = torch.randn((S * chunk, Hq, d), device="cuda").to(dt)
     out = torch.empty_like(q)
-    ms = _events(lambda: pa.prefill(out, q, kc, vc, bt, sl, starts, chunk, case.scale),
+    # bf16: with the workspace the call converts the value rows to fp16 first
+    # (a second kernel, timed with it) and P.V is one product
+    ws = pa.alloc_prefill_workspace(sl, kc, bt) if workspace else None
+    ms = _events(lambda: pa.prefill(out, q, kc, vc, bt, sl, starts, chunk, case.scale, ws),
                  steps, max(3, warmup))
     pairs = S * sum(ctx - chunk + j + 1 for j in range(chunk))
     tf = 4.0 * d * Hq * pairs / (ms * 1e-3) / 1e12
     peak, kind = _bf16_peak()
-    del kc, vc, q, out
+    ws_bytes = 0 if ws is None else ws.numel()
+    del kc, vc, q, out, ws
     torch.cuda.empty_cache()
     return {"value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
             "frac": round(tf / peak, 4), "tokens_per_s": round(S * chunk / (ms * 1e-3), 1),
+            "launches_per_call": 2 if ws_bytes else 1,
             "config": {"sequences": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": d,
-                       "block_size": B, "context": ctx, "chunk": chunk, "dtype": tname}}
+                       "block_size": B, "context": ctx, "chunk": chunk, "dtype": tname,
+                       "workspace_bytes": ws_bytes,
+                       "p_v": "one fp16 product" if (tname == "fp16" or ws_bytes) else
+                              "two bf16 products (weight head + remainder)"}}
 
 
 def prefill_block(steps, warmup, gpu_index):
@@ -752,7 +761,8 @@ def prefill_block(steps, warmup, gpu_index):
         whole = measure_prefill(2048, 2048, 16, "bf16", steps, warmup)
     return {"kernel": "paged_prefill_tc_kernel", "metric": "paged causal prefill TFLOP/s (algorithmic)",
             "bound": "tensor", "peak": peak, "peak_kind": kind, "chunked": chunked,
-            "whole_prompt": whole, "steps": steps, "launches_timed": 2 * steps,
+            "whole_prompt": whole, "steps": steps,
+            "launches_timed": steps * (chunked["launches_per_call"] + whole["launches_per_call"]),
             "clocks": clk.summary()}
 
 
@@ -761,7 +771,8 @@ def run_prefill(args):
     from paged_kv_cache_305_gb300 import build as pbuild
     pbuild.build()
     r = measure_prefill(args.prefill_context, args.prefill_chunk, args.prefill_block_size,
-                        args.prefill_dtype, args.steps, args.warmup)
+                        args.prefill_dtype, args.steps, args.warmup,
+                        workspace=not args.prefill_no_workspace)
     peak, kind = _bf16_peak()
     print(json.dumps({"op": "prefill", "metric": "paged causal prefill TFLOP/s (algorithmic)",
                       "value": r["value"], "unit": "TFLOP/s", "ms_per_call": r["ms_per_call"],
@@ -793,6 +804,8 @@ def main():
     ap.add_argument("--prefill-chunk", type=int, default=2048)
     ap.add_argument("--prefill-block-size", type=int, default=16)
     ap.add_argument("--prefill-dtype", default="bf16", choices=["bf16", "fp16"])
+    ap.add_argument("--prefill-no-workspace", action="store_true",
+                    help="bf16 prefill without its workspace (two P.V products, no fp16 copy of V)")
     ap.add_argument("--graph", action="store_true",
                     help="capture the step (and the end-to-end step) in CUDA graphs and replay them")
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],

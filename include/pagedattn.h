@@ -230,20 +230,38 @@ size_t pa_decode_no_alloc_scratch_bytes(void);
  * Runs on the tcgen05 tensor cores (whole blocks of 8..64 tokens copied by
  * TMA, smaller blocks row by row). num_blocks * block_size must be below 2^31
  * (PA_ERR_UNSUPPORTED otherwise).
- * Arithmetic: q.K in the input type with fp32 accumulation. fp16: every
- * softmax weight enters P.V rounded to fp16, in one product with fp32
- * accumulation, and each row's sum of weights adds exactly those rounded
- * weights, so a weight's rounding error largely cancels between the weighted
- * sum and the sum (the result is off by at most about 2^-11 * max_t |V_t -
- * out| from that rounding). bf16: every weight enters as the sum of two bf16
- * parts (its upper half and the rounding of the remainder, relative error
- * below 2^-16), two products.
+ * Arithmetic: q.K in the input type with fp32 accumulation. fp16 caches,
+ * and bf16 caches given a workspace: every softmax weight enters P.V rounded
+ * to fp16, in one product with fp16 V and fp32 accumulation, and each row's
+ * sum of weights adds exactly those rounded weights, so a weight's rounding
+ * error largely cancels between the weighted sum and the sum (the result is
+ * off by at most about 2^-11 * max_t |V_t - out| from that rounding). For
+ * bf16 the call first converts the value rows of every sequence to an fp16
+ * copy in the workspace (a second kernel on `stream`; a value beyond fp16's
+ * range, +-65504, becomes +-inf there). bf16 without a workspace (NULL):
+ * every weight enters as the sum of two bf16 parts (its upper half and the
+ * rounding of the remainder, relative error below 2^-16), two products, and
+ * no copy is made.
+ * workspace: DEVICE, 16-byte aligned, pa_prefill_workspace_bytes(...) bytes
+ * (contents need no initialisation; calls sharing it must not overlap on the
+ * GPU), or NULL. It is ignored when that size is 0 (fp16 caches).
  */
 int pa_prefill(void* out, const void* query, const void* key_cache, const void* value_cache,
                const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
-               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream);
+               pa_dtype dtype, pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream);
+
+/*
+ * Workspace bytes pa_prefill can use with bf16 caches: an fp16 copy of the
+ * value rows, num_seqs * max_blocks_per_seq * block_size * num_kv_heads *
+ * head_dim * 2 bytes (rounded up to 256). 0 for fp16 caches, for invalid
+ * sizes, and when the copy would have 2^31 slots or more (then pa_prefill
+ * runs without it).
+ */
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int block_size, pa_dtype dtype);
 
 /*
  * Block copies inside the pools, the device half of copy-on-write

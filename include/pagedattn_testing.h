@@ -28,7 +28,8 @@ int pa_testing_prefill_stalled(void* out, const void* query, const void* key_cac
                                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                int block_size, float scale, int max_blocks_per_seq,
                                int num_blocks, int max_query_len, pa_dtype dtype,
-                               pa_dtype out_dtype, cudaStream_t stream);
+                               pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream);
 
 #ifdef __cplusplus
 }

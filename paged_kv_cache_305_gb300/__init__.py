@@ -10,6 +10,7 @@ from .pagedattn import (  # noqa: F401
     PA_ERR_CAPACITY,
     BlockManager,
     PagedAttnError,
+    alloc_prefill_workspace,
     alloc_workspace,
     bad_index_count,
     copy_blocks,
@@ -20,6 +21,7 @@ from .pagedattn import (  # noqa: F401
     last_error,
     load_library,
     prefill,
+    prefill_workspace_bytes,
     no_alloc_scratch_bytes,
     reshape_and_cache,
     testing_prefill_stalled,

@@ -176,6 +176,16 @@ namespace pa {
 int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
 void clear_error() { g_error.clear(); }
 
+size_t prefill_v16_bytes(int num_seqs, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                         int block_size, bool bf16) {
+  if (!bf16 || num_seqs < 1 || num_kv_heads < 1 || (head_dim != 64 && head_dim != 128) ||
+      max_blocks_per_seq < 1 || log2_pow2(block_size) < 0)
+    return 0;
+  const long long slots = static_cast<long long>(num_seqs) * max_blocks_per_seq * block_size;
+  if (slots > 0x7fffffffll) return 0;  // slot numbers are 32-bit in the kernel
+  return round_up(static_cast<size_t>(slots) * num_kv_heads * head_dim * 2, 256);
+}
+
 WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, int max_partitions) {
   WorkspaceLayout w{};
   const size_t rows = static_cast<size_t>(num_seqs) * num_q_heads;
@@ -271,7 +281,8 @@ int prefill_impl(void* out, const void* query, const void* key_cache, const void
                  const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                  float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
-                 pa_dtype dtype, pa_dtype out_dtype, int stall_for_test, cudaStream_t stream) {
+                 pa_dtype dtype, pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+                 int stall_for_test, cudaStream_t stream) {
   g_error.clear();
   int rc = check_dtype(dtype);
   if (rc != PA_OK) return rc;
@@ -300,6 +311,18 @@ int prefill_impl(void* out, const void* query, const void* key_cache, const void
   if (max_query_len < 0) return fail(PA_ERR_INVALID, "max_query_len %d < 0", max_query_len);
   if (num_seqs > 65535 || num_kv_heads > 65535)
     return fail(PA_ERR_UNSUPPORTED, "num_seqs %d / num_kv_heads %d above 65535", num_seqs, num_kv_heads);
+  // bf16 with a workspace: the fp16 copy of the value rows (one P.V product)
+  const size_t v16_need = pa::prefill_v16_bytes(num_seqs, num_kv_heads, head_dim,
+                                                max_blocks_per_seq, block_size,
+                                                dtype == PA_BFLOAT16);
+  void* v16 = nullptr;
+  if (workspace != nullptr && v16_need > 0) {
+    if (workspace_bytes < v16_need)
+      return fail(PA_ERR_WORKSPACE, "prefill workspace of %zu bytes needed, %zu given", v16_need,
+                  workspace_bytes);
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID, "workspace must be 16-byte aligned");
+    v16 = workspace;
+  }
   if (num_seqs == 0 || max_query_len == 0) return PA_OK;
   if (!out || !query || !key_cache || !value_cache || !block_tables || !seq_lens || !query_start)
     return fail(PA_ERR_INVALID, "a pointer argument is NULL");
@@ -329,6 +352,7 @@ int prefill_impl(void* out, const void* query, const void* key_cache, const void
   a.out_f32 = out_dtype == PA_FLOAT32 ? 1 : 0;
   a.bad = bad;
   a.stall_for_test = stall_for_test;
+  a.v16 = v16;
   rc = counter(true, &a.timeouts);
   if (rc != PA_OK) return rc;
   cudaError_t e = pa::launch_prefill_tc(a, head_dim, dtype == PA_BFLOAT16, max_query_len, stream);
@@ -344,10 +368,18 @@ int pa_prefill(void* out, const void* query, const void* key_cache, const void* 
                const int32_t* block_tables, const int32_t* seq_lens, const int32_t* query_start,
                int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                float scale, int max_blocks_per_seq, int num_blocks, int max_query_len,
-               pa_dtype dtype, pa_dtype out_dtype, cudaStream_t stream) {
+               pa_dtype dtype, pa_dtype out_dtype, void* workspace, size_t workspace_bytes,
+               cudaStream_t stream) {
   return prefill_impl(out, query, key_cache, value_cache, block_tables, seq_lens, query_start,
                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale,
-                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, 0, stream);
+                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, workspace,
+                      workspace_bytes, 0, stream);
+}
+
+size_t pa_prefill_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim,
+                                  int max_blocks_per_seq, int block_size, pa_dtype dtype) {
+  return pa::prefill_v16_bytes(num_seqs, num_kv_heads, head_dim, max_blocks_per_seq, block_size,
+                               dtype == PA_BFLOAT16);
 }
 
 int pa_testing_prefill_stalled(void* out, const void* query, const void* key_cache,
@@ -356,10 +388,11 @@ int pa_testing_prefill_stalled(void* out, const void* query, const void* key_cac
                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                float scale, int max_blocks_per_seq, int num_blocks,
                                int max_query_len, pa_dtype dtype, pa_dtype out_dtype,
-                               cudaStream_t stream) {
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   return prefill_impl(out, query, key_cache, value_cache, block_tables, seq_lens, query_start,
                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, scale,
-                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, 1, stream);
+                      max_blocks_per_seq, num_blocks, max_query_len, dtype, out_dtype, workspace,
+                      workspace_bytes, 1, stream);
 }
 
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,

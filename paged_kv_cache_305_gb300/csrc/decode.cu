@@ -149,14 +149,16 @@ paged_decode_kernel(const DecodeArgs a) {
   // by one at run time (claimed through a counter in the workspace) to the
   // CTAs that finish their static share first; the rest of the row (its
   // "lead", at least one partition) is split statically. d is a function of
-  // the data alone: about dyn_percent % of the row's partitions, the
-  // fraction rounded up or down by a fixed per-sequence offset.
+  // the data alone: about dyn_percent % of the partitions of a row of up to
+  // 4 partitions and twice that share of a longer row's, the fraction
+  // rounded up or down by a fixed per-sequence offset.
   auto dyn_of = [&](int np, int s) -> int {
     // long rows (more than kDynMaxParts partitions) keep a static split: they
     // balance well already, and their many pieces would make the merge long
     if (a.dyn_percent <= 0 || np < 2 || np > kDynMaxParts) return 0;
+    const long long pct = np <= 4 ? a.dyn_percent : 2 * a.dyn_percent;
     const long long off = (static_cast<unsigned>(s) * 2654435761u) % 100u;
-    const long long d = (static_cast<long long>(np) * a.dyn_percent + off) / 100;
+    const long long d = (static_cast<long long>(np) * pct + off) / 100;
     return static_cast<int>(min(d, static_cast<long long>(np - 1)));
   };
   struct Lead {
@@ -199,20 +201,28 @@ paged_decode_kernel(const DecodeArgs a) {
     const long long v = __shfl_up_sync(kFull, incl, off);
     if (lane >= off) incl += v;
   }
-  long long dsum = dmine;
+  long long dincl = dmine;  // the same for the dynamic partitions
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) dsum += __shfl_xor_sync(kFull, dsum, off);
+  for (int off = 1; off < 32; off <<= 1) {
+    const long long v = __shfl_up_sync(kFull, dincl, off);
+    if (lane >= off) dincl += v;
+  }
   long long* sScan = reinterpret_cast<long long*>(sPipe);
-  if (lane == 31) sScan[warp] = incl;
-  if (lane == 0) sScan[kWarps + warp] = dsum;
+  if (lane == 31) {
+    sScan[warp] = incl;
+    sScan[kWarps + warp] = dincl;
+  }
   if (tid == 0) {
     sRange[0] = NG; sRange[1] = 0; sRange[2] = 0;
     sRange[3] = NG; sRange[4] = 0; sRange[5] = 0;
     sW[1] = sW[2] = 0;
   }
   __syncthreads();
-  long long base = incl - mine;
-  for (int w = 0; w < warp; ++w) base += sScan[w];
+  long long base = incl - mine, dbase = dincl - dmine;  // this thread's chunk starts
+  for (int w = 0; w < warp; ++w) {
+    base += sScan[w];
+    dbase += sScan[kWarps + w];
+  }
   long long Wseq = 0, Dseq = 0;
   for (int w = 0; w < kWarps; ++w) {
     Wseq += sScan[w];
@@ -328,49 +338,34 @@ paged_decode_kernel(const DecodeArgs a) {
     }
   };
 
-  // one dynamic partition: record of the u-th one (warp 0; in head group
-  // u / Dseq, sequences in order, each row's trailing partitions in order)
+  // one dynamic partition: the record of the u-th one (head group u / Dseq,
+  // sequences in order, each row's trailing partitions in order), written
+  // by the thread whose chunk of sequences holds it
   auto locate_unit = [&](unsigned long long u) {
     const int hg = static_cast<int>(u / static_cast<unsigned long long>(Dseq));
     const long long off = static_cast<long long>(u) - static_cast<long long>(hg) * Dseq;
-    long long acc_d = 0, acc_w = 0;
-    for (int s0 = 0; s0 < S; s0 += 32) {
-      const int s = s0 + lane;
-      Lead ld{0, 0, 0, 0};
-      if (s < S) ld = lead_of(s);
-      long long id = ld.d, iw = ld.w;  // inclusive scans over the 32 sequences
-#pragma unroll
-      for (int k = 1; k < 32; k <<= 1) {
-        const long long vd = __shfl_up_sync(kFull, id, k);
-        const long long vw = __shfl_up_sync(kFull, iw, k);
-        if (lane >= k) {
-          id += vd;
-          iw += vw;
-        }
-      }
-      const long long td = __shfl_sync(kFull, id, 31), tw = __shfl_sync(kFull, iw, 31);
-      if (off < acc_d + td) {  // warp-uniform
-        const long long lo = acc_d + id - ld.d;
-        if (s < S && lo <= off && off < acc_d + id) {
-          const int i = static_cast<int>(off - lo);
-          int me;
-          const int ns = lead_pieces(static_cast<long long>(hg) * Wseq + acc_w + iw - ld.w, ld.npl,
-                                     -1, &me);
-          Seg g;
-          g.s = s;
-          g.hg = hg;
-          g.t0 = (ld.npl + i) * Pt;
-          g.t1 = static_cast<int>(min(static_cast<long long>(g.t0) + Pt, static_cast<long long>(ld.L)));
-          g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
-          g.piece = ns + i;
-          g.npieces = ns + ld.d;
-          g.L = ld.L;
-          sSeg[0] = g;
-        }
+    if (!(dmine > 0 && dbase <= off && off < dbase + dmine)) return;
+    long long acc_d = dbase, acc_w = base;
+    for (int s = s_lo; s < s_hi; ++s) {
+      const Lead ld = lead_of(s);
+      if (off < acc_d + ld.d) {
+        const int i = static_cast<int>(off - acc_d);
+        int me;
+        const int ns = lead_pieces(static_cast<long long>(hg) * Wseq + acc_w, ld.npl, -1, &me);
+        Seg g;
+        g.s = s;
+        g.hg = hg;
+        g.t0 = (ld.npl + i) * Pt;
+        g.t1 = static_cast<int>(min(static_cast<long long>(g.t0) + Pt, static_cast<long long>(ld.L)));
+        g.ntiles = (g.t1 - g.t0 + kTileTokens - 1) / kTileTokens;
+        g.piece = ns + i;
+        g.npieces = ns + ld.d;
+        g.L = ld.L;
+        sSeg[0] = g;
         return;
       }
-      acc_d += td;
-      acc_w += tw;
+      acc_d += ld.d;
+      acc_w += ld.w;
     }
   };
 
@@ -416,7 +411,7 @@ paged_decode_kernel(const DecodeArgs a) {
       __syncthreads();
       const unsigned long long u = sClaim;
       if (u >= static_cast<unsigned long long>(Dtot)) break;  // uniform
-      if (warp == 0) locate_unit(u);
+      locate_unit(u);
       nseg = 1;
     }
     __syncthreads();

@@ -61,7 +61,13 @@ struct PrefillArgs {
   unsigned long long* bad;
   unsigned long long* timeouts;  // bounded waits that gave up (tensor-core kernel)
   int stall_for_test;  // 1: the product thread waits on a barrier nothing signals
+  void* v16;           // bf16 caches: fp16 copy of the value rows [S * MB * B, Hkv, d], or null
 };
+
+// Bytes of the fp16 copy of the value rows the bf16 prefill can use (0 when
+// it does not apply: fp16 caches, or a copy of 2^31 slots or more).
+size_t prefill_v16_bytes(int num_seqs, int num_kv_heads, int head_dim, int max_blocks_per_seq,
+                         int block_size, bool bf16);
 
 // Tensor-core (tcgen05) prefill: block sizes 1..64 (TMA block copies from 8
 // up, 16-byte row copies below), fewer than 2^31 slots.

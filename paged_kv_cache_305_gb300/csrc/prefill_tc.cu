@@ -157,13 +157,22 @@ __device__ __forceinline__ float add_f16x2(float acc, uint32_t h) {
   return acc;
 }
 
+// Two bf16 values to fp16, round to nearest even (exact inside fp16's normal
+// range; beyond +-65504 the result is inf).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return F16::pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // Bounded wait made uniform across the warp: every lane of a warp that
 // executes warp-collective tensor-memory instructions must take the same path.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(kFull, tc::mbar_wait(bar, parity));
 }
 
-template <typename Ty, int D>
+// SINGLE: fp16 weights in one P V product with fp16 V (fp16 caches, or bf16
+// caches whose value rows were first converted to an fp16 copy, v16);
+// otherwise bf16 weights as a head plus the rounding of the remainder.
+template <typename Ty, int D, bool SINGLE>
 __global__ void __launch_bounds__(kThreads, 2)
 paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
@@ -323,14 +332,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           m = mn;
         }
         // weights 2^(s*sl2 - m), the exponent arguments by paired fp32
-        // multiply-adds. fp16 inputs: the fp16 rounding of each weight
-        // (scaled by 2^6), one product with fp16 V, and the row sum adds
-        // exactly those rounded weights, so a weight's rounding error cancels
-        // between the weighted sum and the sum. bf16 inputs: a 16-bit head
-        // (the upper half of the fp32 weight, taken by byte selection) and
-        // the 16-bit rounding of the remainder, two products (the operands of
-        // one product share a type, and V is bf16).
-        constexpr float kOff = Ty::kIsBf16 ? 0.f : kWeightLog2Offset;
+        // multiply-adds. SINGLE: the fp16 rounding of each weight (scaled by
+        // 2^6), one product with fp16 V, and the row sum adds exactly those
+        // rounded weights, so a weight's rounding error cancels between the
+        // weighted sum and the sum. Otherwise (bf16 V): a bf16 head (the
+        // upper half of the fp32 weight, taken by byte selection) and the
+        // bf16 rounding of the remainder, two products (the operands of one
+        // product share a type).
+        constexpr float kOff = SINGLE ? kWeightLog2Offset : 0.f;
         const uint64_t sl2x2 = f2(sl2, sl2), nmx2 = f2(kOff - m, kOff - m);
         float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -342,7 +351,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             arg.y = c + 1 > lim ? -INFINITY : arg.y;
           }
           const float p0 = ex2(arg.x), p1 = ex2(arg.y);
-          if constexpr (Ty::kIsBf16) {
+          if constexpr (!SINGLE) {
             rs[i & 3] += p0;
             rs[i & 3] += p1;
             const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
@@ -350,7 +359,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
             pl[i] = Ty::pack(p0 - __uint_as_float(b0 & 0xffff0000u),
                              p1 - __uint_as_float(b1 & 0xffff0000u));
           } else {
-            ph[i] = Ty::pack(p0, p1);
+            ph[i] = F16::pack(p0, p1);
             rs[i & 3] = add_f16x2(rs[i & 3], ph[i]);
           }
         }
@@ -383,8 +392,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) w[i] = ph[16 * hh + i];
-          tc::tmem_st16(lane_addr + kColP + 16 * hh, w);  // weights (bf16: head part)
-          if constexpr (Ty::kIsBf16) {
+          tc::tmem_st16(lane_addr + kColP + 16 * hh, w);  // weights (two products: head part)
+          if constexpr (!SINGLE) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) w[i] = pl[16 * hh + i];
             tc::tmem_st16(lane_addr + kColP + 32 + 16 * hh, w);  // weights, remainder
@@ -431,7 +440,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   } else if (warp == kKWarp || warp == kVWarp) {
     // ---------------- producers: K (or V) tiles of 64 tokens through the block table
     const bool is_v = warp == kVWarp;
-    const T* cache = static_cast<const T*>(is_v ? a.value_cache : a.key_cache);
+    // bf16 caches with SINGLE: the V tiles come from the fp16 copy of the
+    // value rows that the conversion pass wrote, block blk of sequence s at
+    // block s * max_blocks_per_seq + blk (rejected block ids there are zeros)
+    const bool from_v16 = SINGLE && Ty::kIsBf16 && is_v;
+    const T* cache = static_cast<const T*>(from_v16 ? a.v16 : (is_v ? a.value_cache : a.key_cache));
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     const int full0 = is_v ? kBarVFull : kBarKFull;
     const int empty0 = is_v ? kBarODone : kBarSFull;  // stage free once S_j / P_j V is done
@@ -449,10 +462,14 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
         const int blk = jt * nb + lane;
         valid = min(max(L - (blk << shift), 0), B);
         if (valid > 0) {
-          id = __ldg(trow + blk);
-          if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
-            if (!is_v) atomicAdd(a.bad, 1ull);  // counted once, by the K producer
-            id = -1;
+          if (from_v16) {
+            id = s * a.max_blocks_per_seq + blk;
+          } else {
+            id = __ldg(trow + blk);
+            if (static_cast<unsigned>(id) >= static_cast<unsigned>(a.num_blocks)) {
+              if (!is_v) atomicAdd(a.bad, 1ull);  // counted once, by the K producer
+              id = -1;
+            }
           }
         }
       }
@@ -516,11 +533,15 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
           const int t = jt * kKeys + lane + 32 * u;
           sr[u] = -1;
           if (jt < ntiles && t < L) {
-            const int id = __ldg(trow + (t >> shift));
-            if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
-              sr[u] = (id << shift) + (t & (B - 1));
-            else if (!is_v && (t & (B - 1)) == 0)
-              atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
+            if (from_v16) {
+              sr[u] = ((s * a.max_blocks_per_seq + (t >> shift)) << shift) + (t & (B - 1));
+            } else {
+              const int id = __ldg(trow + (t >> shift));
+              if (static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks))
+                sr[u] = (id << shift) + (t & (B - 1));
+              else if (!is_v && (t & (B - 1)) == 0)
+                atomicAdd(a.bad, 1ull);  // counted once per block, by the K producer
+            }
           }
         }
       };
@@ -578,7 +599,8 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // ---------------- products, one thread; descriptors built once, moved by
     // adding (byte offset >> 4) to the start-address field
     const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
-    const uint32_t id_o = tc::idesc_f16(kRows, D, Ty::kIsBf16, true);
+    // P V: fp16 weights with fp16 V, or bf16 weight parts with bf16 V
+    const uint32_t id_o = tc::idesc_f16(kRows, D, SINGLE ? false : Ty::kIsBf16, true);
     const uint64_t dq0 = tc::sdesc_sw128(sQ, 16, 1024);
     // K read K-major: 8-token groups kGroupBytes apart (SBO)
     const uint64_t dk0 = tc::sdesc_sw128(sK(0), 16, Geo::kGroupBytes);
@@ -634,7 +656,7 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
       const uint64_t dv = dv0 + b * kStageStep;
       // fp16: one product; bf16: the weights' head part, then the remainder
 #pragma unroll
-      for (int part = 0; part < (Ty::kIsBf16 ? 2 : 1); ++part) {
+      for (int part = 0; part < (SINGLE ? 1 : 2); ++part) {
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks)
           tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
@@ -654,6 +676,41 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
   if (warp == 0) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Conversion pass for bf16 caches: the value rows of every sequence, in
+// logical order, to an fp16 copy: block j of sequence s (its B slots x Hkv x
+// d) at block s * max_blocks_per_seq + j of v16, so the prefill's V tiles are
+// fp16 and P V is one product. One CTA per (block j, sequence s); only the
+// rows before the sequence's length are written (the prefill reads no
+// others); a rejected block id gives zero rows (the prefill's K producer
+// counts it). Values beyond fp16's range become +-inf.
+template <int D>
+__global__ void __launch_bounds__(256) v16_convert_kernel(const PrefillArgs a) {
+  const int j = blockIdx.x, s = blockIdx.y;
+  const int shift = a.block_shift;
+  const int B = 1 << shift;
+  const int Lmax = a.max_blocks_per_seq << shift;
+  const int L = min(max(a.seq_lens[s], 0), Lmax);
+  const int rows = min(L - (j << shift), B);
+  if (rows <= 0) return;
+  const int id = __ldg(a.block_tables + static_cast<size_t>(s) * a.max_blocks_per_seq + j);
+  const bool ok = static_cast<unsigned>(id) < static_cast<unsigned>(a.num_blocks);
+  const size_t row_chunks = static_cast<size_t>(a.num_kv_heads) * D / 8;  // 16-byte chunks per slot
+  const size_t n = static_cast<size_t>(rows) * row_chunks;
+  const uint4* src = reinterpret_cast<const uint4*>(a.value_cache) +
+                     (static_cast<size_t>(ok ? id : 0) << shift) * row_chunks;
+  uint4* dst = reinterpret_cast<uint4*>(a.v16) +
+               ((static_cast<size_t>(s) * a.max_blocks_per_seq + j) << shift) * row_chunks;
+  for (size_t i = threadIdx.x; i < n; i += 256) {
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (ok) {
+      const uint4 v = __ldg(src + i);
+      w = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                     bf16x2_to_f16x2(v.w));
+    }
+    dst[i] = w;
   }
 }
 
@@ -700,24 +757,41 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, long long 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename Ty, int D>
-cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stream) {
-  const int P = kRows / a.group;
-  const int tiles = (max_query_len + P - 1) / P;
-  if (tiles < 1) return cudaSuccess;
-  const long long slots = static_cast<long long>(a.num_blocks) << a.block_shift;
-  CUtensorMap km, vm;
-  if (!encode_cache_map(&km, a.key_cache, Ty::kIsBf16, slots, a.num_kv_heads, D,
-                        1 << a.block_shift) ||
-      !encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, slots, a.num_kv_heads, D,
-                        1 << a.block_shift))
-    return cudaErrorInvalidValue;
-  auto kern = paged_prefill_tc_kernel<Ty, D>;
+template <typename Ty, int D, bool SINGLE>
+cudaError_t launch_kernel(const CUtensorMap& km, const CUtensorMap& vm, const PrefillArgs& a,
+                          int tiles, cudaStream_t stream) {
+  auto kern = paged_prefill_tc_kernel<Ty, D, SINGLE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<D>::kSmem);
   if (e != cudaSuccess) return e;
   kern<<<dim3(tiles, a.num_kv_heads, a.num_seqs), kThreads, TcGeo<D>::kSmem, stream>>>(km, vm, a);
   return cudaGetLastError();
+}
+
+template <typename Ty, int D>
+cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stream) {
+  const int P = kRows / a.group;
+  const int tiles = (max_query_len + P - 1) / P;
+  if (tiles < 1) return cudaSuccess;
+  const int B = 1 << a.block_shift;
+  const long long slots = static_cast<long long>(a.num_blocks) << a.block_shift;
+  CUtensorMap km, vm;
+  if (!encode_cache_map(&km, a.key_cache, Ty::kIsBf16, slots, a.num_kv_heads, D, B))
+    return cudaErrorInvalidValue;
+  if (Ty::kIsBf16 && a.v16 != nullptr) {
+    // bf16 with a workspace: the value rows to fp16 first, then one P V product
+    const long long vslots =
+        static_cast<long long>(a.num_seqs) * a.max_blocks_per_seq << a.block_shift;
+    if (!encode_cache_map(&vm, a.v16, false, vslots, a.num_kv_heads, D, B))
+      return cudaErrorInvalidValue;
+    v16_convert_kernel<D><<<dim3(a.max_blocks_per_seq, a.num_seqs), 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_kernel<Ty, D, true>(km, vm, a, tiles, stream);
+  }
+  if (!encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, slots, a.num_kv_heads, D, B))
+    return cudaErrorInvalidValue;
+  return launch_kernel<Ty, D, !Ty::kIsBf16>(km, vm, a, tiles, stream);
 }
 
 }  // namespace

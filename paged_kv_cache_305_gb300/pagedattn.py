@@ -24,7 +24,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
             "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
             "pa_decode_append", "pa_prefill", "pa_wait_timeout_count",
-            "pa_testing_prefill_stalled")
+            "pa_testing_prefill_stalled", "pa_prefill_workspace_bytes")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -69,7 +69,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                    ctypes.c_float, i32, i32, i32, i32, i32, vp, sz, vp]
     L.pa_decode_append.restype = i32
     L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
-                             i32, i32, i32, i32, i32, vp]
+                             i32, i32, i32, i32, i32, vp, sz, vp]
+    L.pa_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+    L.pa_prefill_workspace_bytes.restype = sz
     L.pa_prefill.restype = i32
     L.pa_testing_prefill_stalled.argtypes = L.pa_prefill.argtypes
     L.pa_testing_prefill_stalled.restype = i32
@@ -239,10 +241,31 @@ def decode_append(out: torch.Tensor, query: torch.Tensor, new_key: torch.Tensor,
     return out
 
 
+def prefill_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int,
+                            max_blocks_per_seq: int, block_size: int, dtype) -> int:
+    """Bytes of the optional :func:`prefill` workspace (an fp16 copy of the value
+    rows for bf16 caches; 0 for fp16). ``dtype``: "bf16"/"fp16" or a torch dtype."""
+    code = {"fp16": PA_FLOAT16, "bf16": PA_BFLOAT16, torch.float16: PA_FLOAT16,
+            torch.bfloat16: PA_BFLOAT16}[dtype]
+    return int(load_library().pa_prefill_workspace_bytes(num_seqs, num_kv_heads, head_dim,
+                                                         max_blocks_per_seq, block_size, code))
+
+
+def alloc_prefill_workspace(seq_lens: torch.Tensor, key_cache: torch.Tensor,
+                            block_tables: torch.Tensor) -> Optional[torch.Tensor]:
+    """Workspace for :func:`prefill` with these shapes (None when it needs none).
+    Its contents need no initialisation."""
+    NB, B, Hkv, d = key_cache.shape
+    n = prefill_workspace_bytes(seq_lens.shape[0], Hkv, d, block_tables.shape[1], B, key_cache.dtype)
+    if n == 0:
+        return None
+    return torch.empty(n, dtype=torch.uint8, device=key_cache.device)
+
+
 def _prefill(entry, out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
             value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
             query_start: torch.Tensor, max_query_len: int, scale: float,
-            stream=None) -> torch.Tensor:
+            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     total_q, Hq, d = query.shape
     NB, B, Hkv, d2 = key_cache.shape
     S = seq_lens.shape[0]
@@ -254,13 +277,17 @@ def _prefill(entry, out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
     _need(block_tables.shape[0] == S and query_start.shape == (S + 1,), "shape mismatch")
     for t in (out, query, key_cache, value_cache, block_tables, seq_lens, query_start):
         _need(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        _need(workspace.is_cuda and workspace.is_contiguous(), "workspace must be a contiguous CUDA tensor")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     L = load_library()
     with torch.cuda.device(query.device):
         _check(getattr(L, entry)(
             out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
             block_tables.data_ptr(), seq_lens.data_ptr(), query_start.data_ptr(), S, Hq, Hkv, d, B,
             float(scale), block_tables.shape[1], NB, int(max_query_len), _dtype_code(query),
-            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query),
+            PA_FLOAT32 if out.dtype == torch.float32 else _dtype_code(query), ws_ptr, ws_bytes,
             _stream(query, stream)))
     return out
 
@@ -268,27 +295,30 @@ def _prefill(entry, out: torch.Tensor, query: torch.Tensor, key_cache: torch.Ten
 def prefill(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
             value_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
             query_start: torch.Tensor, max_query_len: int, scale: float,
-            stream=None) -> torch.Tensor:
+            workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Causal attention of each sequence's newest tokens over the paged cache.
 
     ``query``/``out`` [total_q, Hq, d]; sequence s owns query rows
     query_start[s] .. query_start[s+1]-1 (int32 [S+1]), its newest tokens,
     whose K/V are already in the cache; ``max_query_len`` bounds the rows per
-    sequence.
+    sequence. ``workspace`` (optional, :func:`alloc_prefill_workspace`): with
+    bf16 caches the value rows are converted to an fp16 copy there and P.V is
+    one fp16 product; without it bf16 takes two products.
     """
     return _prefill("pa_prefill", out, query, key_cache, value_cache, block_tables, seq_lens,
-                    query_start, max_query_len, scale, stream)
+                    query_start, max_query_len, scale, workspace, stream)
 
 
 def testing_prefill_stalled(out: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                             value_cache: torch.Tensor, block_tables: torch.Tensor,
                             seq_lens: torch.Tensor, query_start: torch.Tensor, max_query_len: int,
-                            scale: float, stream=None) -> torch.Tensor:
+                            scale: float, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
     """Test hook (include/pagedattn_testing.h): :func:`prefill` whose product
     thread waits on a barrier nothing signals, so bounded waits give up and
     the launch winds down; ``out`` is left unwritten."""
     return _prefill("pa_testing_prefill_stalled", out, query, key_cache, value_cache,
-                    block_tables, seq_lens, query_start, max_query_len, scale, stream)
+                    block_tables, seq_lens, query_start, max_query_len, scale, workspace, stream)
 
 
 def bad_index_count(clear: bool = False) -> int:

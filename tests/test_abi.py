@@ -166,11 +166,12 @@ def test_cache_write_zero_tokens_is_a_no_op(lib):
 
 def _prefill(lib, **kw):
     a = dict(out=FAKE, query=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, sl=FAKE, qs=FAKE, S=2, Hq=8, Hkv=2,
-             d=128, B=16, scale=0.1, MB=4, NB=100, mq=64, dtype=1, odt=None)
+             d=128, B=16, scale=0.1, MB=4, NB=100, mq=64, dtype=1, odt=None, ws=None, wsb=0)
     a.update(kw)
     return lib.pa_prefill(a["out"], a["query"], a["kc"], a["vc"], a["bt"], a["sl"], a["qs"], a["S"],
                           a["Hq"], a["Hkv"], a["d"], a["B"], a["scale"], a["MB"], a["NB"], a["mq"],
-                          a["dtype"], a["dtype"] if a["odt"] is None else a["odt"], None)
+                          a["dtype"], a["dtype"] if a["odt"] is None else a["odt"], a["ws"], a["wsb"],
+                          None)
 
 
 @pytest.mark.parametrize("kw,code,msg", [
@@ -188,10 +189,25 @@ def _prefill(lib, **kw):
     (dict(qs=None), -1, "NULL"),
     (dict(out=FAKE + 8), -1, "aligned"),
     (dict(qs=FAKE + 2), -1, "aligned"),
+    (dict(ws=FAKE, wsb=64), -3, "workspace"),
+    (dict(ws=FAKE + 8, wsb=1 << 30), -1, "aligned"),
 ])
 def test_prefill_rejects_bad_arguments(lib, kw, code, msg):
     assert _prefill(lib, **kw) == code
     assert msg in pa.last_error()
+
+
+def test_prefill_workspace_bytes(lib):
+    # bf16: an fp16 copy of every sequence's value rows, S * MB * B * Hkv * d * 2
+    # bytes rounded up to 256; fp16 needs none; a copy of 2^31 slots or more is
+    # not offered
+    assert pa.prefill_workspace_bytes(16, 8, 128, 256, 16, "bf16") == 16 * 256 * 16 * 8 * 128 * 2
+    assert pa.prefill_workspace_bytes(3, 1, 64, 5, 1, "bf16") == 2048  # 1920 rounded up
+    assert pa.prefill_workspace_bytes(16, 8, 128, 256, 16, "fp16") == 0
+    assert pa.prefill_workspace_bytes(4096, 8, 128, 1 << 16, 16, "bf16") == 0
+    assert pa.prefill_workspace_bytes(4, 8, 96, 16, 16, "bf16") == 0
+    # an fp16 call ignores a workspace it cannot use
+    assert _prefill(lib, dtype=0, ws=FAKE, wsb=64, S=0, out=None) == 0
 
 
 def test_prefill_empty_calls_are_no_ops(lib):

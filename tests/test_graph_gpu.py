@@ -52,7 +52,10 @@ def test_captured_decode_step_replays_bit_identically(name):
     assert pa.bad_index_count(clear=True) == 0
 
 
-def test_captured_prefill_replays_bit_identically():
+@pytest.mark.parametrize("workspace", [True, False])
+def test_captured_prefill_replays_bit_identically(workspace):
+    # with a workspace the call is two kernels (the fp16 copy of the value
+    # rows, then the prefill); both are captured
     case = W.random_case(num_seqs=4, num_q_heads=16, num_kv_heads=4, head_dim=128, block_size=16,
                          len_range=(100, 600), dtype="bf16", seed=9)
     qlens = [int(x) for x in np.minimum(case.seq_lens, 200)]
@@ -61,10 +64,11 @@ def test_captured_prefill_replays_bit_identically():
     dc = DeviceCase(case)
     qs = torch.from_numpy(starts).cuda()
     out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    ws = pa.alloc_prefill_workspace(dc.seq_lens, dc.key_cache, dc.block_tables) if workspace else None
 
     def call():
         pa.prefill(out, q, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs,
-                   max(qlens), case.scale)
+                   max(qlens), case.scale, ws)
 
     call()
     torch.cuda.synchronize()

@@ -25,7 +25,12 @@ def _cuda():
     torch.cuda.synchronize()
 
 
-def _run(case, qlens, seed, scale=None):
+def _ws(dc, use=True):
+    """The prefill workspace (bf16: fp16 copy of the value rows), or None."""
+    return pa.alloc_prefill_workspace(dc.seq_lens, dc.key_cache, dc.block_tables) if use else None
+
+
+def _run(case, qlens, seed, scale=None, workspace=True):
     starts = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
     q = W.normal_bits((int(starts[-1]), case.num_q_heads, case.head_dim), case.dtype, seed, 55)
     dc = DeviceCase(case)
@@ -35,8 +40,9 @@ def _run(case, qlens, seed, scale=None):
     out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
     mq = int(max(qlens))
     sc = case.scale if scale is None else scale
-    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc)
-    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc)
+    ws = _ws(dc, workspace)
+    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc, ws)
+    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, mq, sc, ws)
     ref = oracle.paged_prefill(q, case.key_cache, case.value_cache, case.block_tables, case.seq_lens,
                                starts, case.block_size, sc, case.dtype)
     assert pa.wait_timeout_count(clear=True) == 0
@@ -59,14 +65,19 @@ CASES = [
 
 
 @pytest.mark.parametrize("idx", range(len(CASES)))
-def test_prefill_chunks(idx):
+@pytest.mark.parametrize("workspace", [True, False])
+def test_prefill_chunks(idx, workspace):
+    # bf16 with a workspace: the value rows converted to fp16, one P.V
+    # product; without: the two-product path (fp16 needs no workspace)
     dtype, d, Hq, Hkv, B, lens = CASES[idx]
+    if dtype == "fp16" and not workspace:
+        pytest.skip("fp16 takes no workspace")
     case = W.random_case(num_seqs=5, num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, block_size=B,
                          len_range=lens, dtype=dtype, seed=400 + idx)
     L = case.seq_lens
     # a whole prompt, one token, a partial chunk, a zero-length chunk, a ragged chunk
     qlens = [int(L[0]), 1, max(1, int(L[2]) // 3), 0, min(int(L[4]), 77)]
-    _run(case, qlens, idx)
+    _run(case, qlens, idx, workspace=workspace)
 
 
 def test_single_token_chunks_match_decode():
@@ -126,7 +137,7 @@ def test_bad_block_ids_are_counted_not_faulted(B):
     out = torch.empty((30, 8, 128), dtype=torch.float32, device="cuda")
     pa.bad_index_count(clear=True)
     pa.prefill(out, q, dc.key_cache, dc.value_cache, bt, dc.seq_lens, torch.from_numpy(starts).cuda(),
-               10, case.scale)
+               10, case.scale, _ws(dc))
     assert pa.bad_index_count(clear=True) >= 2
     assert pa.wait_timeout_count(clear=True) == 0
     assert torch.isfinite(out).all()
@@ -155,10 +166,11 @@ def test_repeated_calls_are_bit_identical(B):
     starts = torch.from_numpy(np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)).cuda()
     dc = DeviceCase(case)
     qd = dev_bits(q0, "bf16")
+    ws = _ws(dc)
     for _ in range(24):
         out = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
         pa.prefill(out, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, starts,
-                   max(qlens), case.scale)
+                   max(qlens), case.scale, ws)
         assert np.array_equal(out.cpu().numpy(), first)
     assert pa.wait_timeout_count(clear=True) == 0
 
@@ -177,12 +189,13 @@ def test_full_size_chunked_prefill_sampled():
     out32 = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
     out16 = torch.empty_like(qd)
     qs = torch.from_numpy(starts).cuda()
-    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale)
-    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale)
+    ws = _ws(dc)
+    pa.prefill(out32, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale, ws)
+    pa.prefill(out16, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, qs, chunk, case.scale, ws)
     assert pa.wait_timeout_count(clear=True) == 0
     got32 = out32.cpu().numpy()
     got16 = host_bits(out16)
-    del dc, qd, out32, out16
+    del dc, qd, out32, out16, ws
     torch.cuda.empty_cache()
     assert np.all(np.isfinite(got32))
     assert np.array_equal(oracle.round_to_dtype(got32.astype(np.float64), "bf16"), got16)
@@ -220,12 +233,13 @@ def test_a_wait_that_runs_out_is_counted_and_the_device_stays_usable(B):
     qd = dev_bits(q0, "bf16")
     pa.wait_timeout_count(clear=True)
     stalled = torch.full(qd.shape, 7.0, dtype=torch.float32, device="cuda")
+    ws = _ws(dc)
     pa.testing_prefill_stalled(stalled, qd, dc.key_cache, dc.value_cache, dc.block_tables,
-                               dc.seq_lens, starts, max(qlens), case.scale)
+                               dc.seq_lens, starts, max(qlens), case.scale, ws)
     assert pa.wait_timeout_count(clear=True) >= 1
     assert bool((stalled == 7.0).all())  # no product ran, nothing was stored
     out = torch.empty(qd.shape, dtype=torch.float32, device="cuda")
     pa.prefill(out, qd, dc.key_cache, dc.value_cache, dc.block_tables, dc.seq_lens, starts,
-               max(qlens), case.scale)
+               max(qlens), case.scale, ws)
     assert np.array_equal(out.cpu().numpy(), fresh)
     assert pa.wait_timeout_count(clear=True) == 0
