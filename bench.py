@@ -260,13 +260,16 @@ def run_reference(args, rank, world):
 
 
 def _config(case, args):
+    import paged_kv_cache_305_gb300 as pa
+    pt = args.partition_tokens if args.partition_tokens is not None else case.partition_tokens
     return {"workload": case.name, "num_seqs": case.num_seqs, "num_q_heads": case.num_q_heads,
             "num_kv_heads": case.num_kv_heads, "head_dim": case.head_dim,
             "block_size": case.block_size, "seq_len_range": [int(case.seq_lens.min()),
                                                              int(case.seq_lens.max())],
             "mean_seq_len": round(float(case.seq_lens.mean()), 1),
-            "partition_tokens": (args.partition_tokens if args.partition_tokens is not None
-                                 else case.partition_tokens) or 512,
+            # the length the library resolves (0 asks for its default)
+            "partition_tokens": pa.decode_partition_tokens(pt, case.block_size,
+                                                           case.max_blocks_per_seq),
             "kv_bytes_per_step": case.kv_bytes(),
             "step": "write each sequence's newest K/V row into its slot, then decode attention "
                     "over every sequence",

@@ -84,7 +84,7 @@ int pa_reshape_and_cache(const void* key, const void* value,
  * Workspace bytes pa_decode needs for these sizes (0 when one partition
  * covers the longest possible sequence, max_blocks_per_seq * block_size).
  * partition_tokens is the value that will be passed to pa_decode (0 = the
- * library's default, 512 tokens). Returns 0 for invalid sizes.
+ * library's default, see pa_decode). Returns 0 for invalid sizes.
  *
  * Workspace contents: per-(sequence, kv-head) arrival counters at the start,
  * followed by fp32 partial results. Zero-fill a new workspace once, at
@@ -101,6 +101,14 @@ int pa_reshape_and_cache(const void* key, const void* value,
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size,
                                  int partition_tokens);
+
+/*
+ * The split-K partition length pa_decode uses for these arguments: the
+ * default for partition_tokens = 0 (see pa_decode), else partition_tokens
+ * itself. Host-only. Returns PA_ERR_INVALID or PA_ERR_UNSUPPORTED (negative)
+ * where pa_decode would reject the value, with pa_last_error set.
+ */
+int pa_decode_partition_tokens(int partition_tokens, int block_size, int max_blocks_per_seq);
 
 /*
  * Decode attention. For every sequence s and query head hq, with
@@ -125,12 +133,17 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
  * scratch space and the stream.
  *
  * Split-K: each sequence is cut into partitions of partition_tokens tokens
- * (0 = default 512; otherwise a multiple of 16 and of block_size, at most
- * 2^20). The kernel is persistent (a few CTAs per SM); each CTA takes a
- * contiguous, token-balanced run of partitions and continues the online
- * softmax across consecutive partitions of one (sequence, kv head). Where a
- * sequence's partitions are split between CTAs, the pieces are combined by
- * log-sum-exp inside the same launch, so the call is a single kernel.
+ * (0 = the default: 1024 when max_blocks_per_seq * block_size >= 4096, else
+ * 512; otherwise a multiple of 16 and of block_size, at most 2^20). The
+ * kernel is persistent (a few CTAs per SM); each CTA takes a contiguous,
+ * token-balanced run of the rows' leading partitions and continues the
+ * online softmax across consecutive partitions of one (sequence, kv head);
+ * a share of each row's trailing partitions, fixed by the row's length
+ * alone, is claimed at run time from a counter in the workspace. Where a
+ * row is split into pieces, the pieces are numbered by the data alone and
+ * combined by log-sum-exp in piece order inside the same launch, so the call
+ * is a single kernel and its result does not depend on which CTA computed
+ * which piece.
  * `workspace` must hold pa_decode_workspace_bytes(...) bytes (it may be NULL
  * when that is 0); see there for the zeroing rule.
  *

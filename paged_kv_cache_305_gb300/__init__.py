@@ -17,6 +17,7 @@ from .pagedattn import (  # noqa: F401
     decode,
     decode_append,
     decode_no_alloc,
+    decode_partition_tokens,
     decode_workspace_bytes,
     last_error,
     load_library,

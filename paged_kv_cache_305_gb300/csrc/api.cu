@@ -6,6 +6,7 @@
 #include <stdarg.h>
 #include <stdio.h>
 
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -16,7 +17,8 @@
 #include "pagedattn_testing.h"
 
 // Share (%) of every row's partitions that the decode kernel hands out at run
-// time (0: the whole split is static).
+// time, for 512-token partitions, scaled with the partition length (0: the
+// whole split is static).
 #ifndef PA_DECODE_DYNAMIC_PERCENT
 #define PA_DECODE_DYNAMIC_PERCENT pa::kDynamicPercent
 #endif
@@ -115,8 +117,12 @@ int check_dtype(pa_dtype dtype) {
   return PA_OK;
 }
 
-int resolve_partition(int partition_tokens, int block_size, int* pt) {
-  int p = partition_tokens == 0 ? pa::kDefaultPartitionTokens : partition_tokens;
+int resolve_partition(int partition_tokens, int block_size, int max_blocks_per_seq, int* pt) {
+  int p = partition_tokens;
+  if (p == 0)
+    p = static_cast<long long>(max_blocks_per_seq) * block_size >= pa::kLongContextTokens
+            ? pa::kLongPartitionTokens
+            : pa::kDefaultPartitionTokens;
   if (p < 0) return fail(PA_ERR_INVALID, "partition_tokens %d < 0", partition_tokens);
   if (p % 16 != 0 || p % block_size != 0)
     return fail(PA_ERR_INVALID, "partition_tokens %d must be a multiple of 16 and of block_size %d",
@@ -395,6 +401,17 @@ int pa_testing_prefill_stalled(void* out, const void* query, const void* key_cac
                       workspace_bytes, 1, stream);
 }
 
+int pa_decode_partition_tokens(int partition_tokens, int block_size, int max_blocks_per_seq) {
+  g_error.clear();
+  if (log2_pow2(block_size) < 0)
+    return fail(PA_ERR_INVALID, "block_size %d is not a power of two in [1, 64]", block_size);
+  if (max_blocks_per_seq < 1)
+    return fail(PA_ERR_INVALID, "max_blocks_per_seq %d < 1", max_blocks_per_seq);
+  int pt = 0;
+  const int rc = resolve_partition(partition_tokens, block_size, max_blocks_per_seq, &pt);
+  return rc == PA_OK ? pt : rc;
+}
+
 size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
                                  int max_blocks_per_seq, int block_size, int partition_tokens) {
   if (num_seqs < 0 || num_q_heads < 1 || (head_dim != 64 && head_dim != 128) ||
@@ -402,7 +419,7 @@ size_t pa_decode_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
     return 0;
   int pt = 0;
   std::string saved = g_error;
-  if (resolve_partition(partition_tokens, block_size, &pt) != PA_OK) {
+  if (resolve_partition(partition_tokens, block_size, max_blocks_per_seq, &pt) != PA_OK) {
     g_error = saved;
     return 0;
   }
@@ -449,7 +466,7 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
     return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size is 2^32 - 1 slots or more");
   if (!isfinite(scale)) return fail(PA_ERR_INVALID, "scale is not finite");
   int pt = 0;
-  rc = resolve_partition(partition_tokens, block_size, &pt);
+  rc = resolve_partition(partition_tokens, block_size, max_blocks_per_seq, &pt);
   if (rc != PA_OK) return rc;
   const long long lmax = static_cast<long long>(max_blocks_per_seq) * block_size;
   if (lmax > 0x7fffffffll)
@@ -524,7 +541,8 @@ int decode_impl(void* out, const void* query, const void* key_cache, const void*
   // workspace (its header holds the claim counter)
   a.ws_claim = wl.total ? reinterpret_cast<unsigned long long*>(ws) : nullptr;
   a.ws_done = wl.total ? reinterpret_cast<unsigned*>(ws + 8) : nullptr;
-  a.dyn_percent = wl.total ? PA_DECODE_DYNAMIC_PERCENT : 0;
+  // the share grows with the partition length (fewer, larger units per row)
+  a.dyn_percent = wl.total ? std::min(50, PA_DECODE_DYNAMIC_PERCENT * pt / 512) : 0;
   a.ws_lse = wl.total ? reinterpret_cast<float*>(ws + wl.lse_off) : nullptr;
   a.ws_out = wl.total ? reinterpret_cast<float*>(ws + wl.out_off) : nullptr;
   a.bad = bad;

@@ -7,7 +7,12 @@
 
 namespace pa {
 
+// Default split-K partition: 512 tokens, 1024 when the table can address
+// kLongContextTokens or more (long rows: half the pieces and merges, and
+// rows still have several partitions to balance).
 constexpr int kDefaultPartitionTokens = 512;
+constexpr int kLongPartitionTokens = 1024;
+constexpr long long kLongContextTokens = 4096;
 constexpr int kMaxPartitionTokens = 1 << 20;
 constexpr int kMaxGroup = 16;  // query heads per kv head (rows of one mma tile)
 

@@ -24,7 +24,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_bytes", "pa_decode",
             "pa_bm_destroy", "pa_bm_new_sequence", "pa_bm_fork", "pa_bm_free_sequence",
             "pa_bm_append", "pa_bm_block_tables", "pa_bm_num_free_blocks", "pa_bm_ref_count",
             "pa_decode_append", "pa_prefill", "pa_wait_timeout_count",
-            "pa_testing_prefill_stalled", "pa_prefill_workspace_bytes")
+            "pa_testing_prefill_stalled", "pa_prefill_workspace_bytes",
+            "pa_decode_partition_tokens")
 PA_ERR_CAPACITY = -5
 
 _lib = None
@@ -51,6 +52,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     L.pa_reshape_and_cache.restype = i32
     L.pa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
     L.pa_decode_workspace_bytes.restype = sz
+    L.pa_decode_partition_tokens.argtypes = [i32, i32, i32]
+    L.pa_decode_partition_tokens.restype = i32
     L.pa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_float,
                             i32, i32, i32, i32, i32, vp, sz, vp]
     L.pa_decode.restype = i32
@@ -152,6 +155,16 @@ def decode_workspace_bytes(num_seqs: int, num_q_heads: int, head_dim: int,
     return int(load_library().pa_decode_workspace_bytes(num_seqs, num_q_heads, head_dim,
                                                         max_blocks_per_seq, block_size,
                                                         partition_tokens))
+
+
+def decode_partition_tokens(partition_tokens: int, block_size: int,
+                            max_blocks_per_seq: int) -> int:
+    """The split-K partition length pa_decode resolves these arguments to."""
+    rc = load_library().pa_decode_partition_tokens(partition_tokens, block_size,
+                                                   max_blocks_per_seq)
+    if rc < 0:
+        raise PagedAttnError(rc, last_error())
+    return int(rc)
 
 
 def alloc_workspace(query: torch.Tensor, key_cache: torch.Tensor, block_tables: torch.Tensor,

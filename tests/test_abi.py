@@ -77,7 +77,9 @@ def test_workspace_bytes_arithmetic(lib):
     # a 256-byte header (claim counter, finished CTAs), S * Hq counters, then
     # S * Hq * P lse values, then S * Hq * P * d outputs (fp32)
     def expect(S, Hq, d, MB, B, pt):
-        P = -(-(MB * B) // (pt or 512))
+        # partition_tokens 0: 1024 when the table addresses 4096+ tokens, else 512
+        default = 1024 if MB * B >= 4096 else 512
+        P = -(-(MB * B) // (pt or default))
         if P <= 1:
             return 0
         r = lambda x: -(-x // 256) * 256
@@ -86,6 +88,15 @@ def test_workspace_bytes_arithmetic(lib):
     for args in [(128, 32, 128, 512, 16, 0), (8, 64, 128, 8192, 16, 512), (4, 4, 64, 8, 16, 0),
                  (3, 6, 64, 40, 1, 16), (256, 32, 128, 24, 64, 64)]:
         assert pa.decode_workspace_bytes(*args) == expect(*args), args
+    # the partition length the call resolves: 0 asks for the default
+    assert pa.decode_partition_tokens(0, 16, 512) == 1024  # table addresses 8192 tokens
+    assert pa.decode_partition_tokens(0, 16, 256) == 1024  # 4096
+    assert pa.decode_partition_tokens(0, 16, 255) == 512
+    assert pa.decode_partition_tokens(0, 64, 24) == 512
+    assert pa.decode_partition_tokens(768, 16, 512) == 768
+    for bad in [(24, 16, 8), (-16, 16, 8), (0, 3, 8), (0, 16, 0), (64, 128, 8)]:
+        with pytest.raises(pa.PagedAttnError):
+            pa.decode_partition_tokens(*bad)
     # invalid sizes give 0
     assert pa.decode_workspace_bytes(4, 4, 96, 8, 16, 0) == 0
     assert pa.decode_workspace_bytes(4, 4, 64, 8, 3, 0) == 0
