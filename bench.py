@@ -57,8 +57,9 @@ def _peaks():
     return 6800.0, "fallback"
 
 
-def _traffic(workload: str):
-    """DRAM bytes per decode launch from a committed ncu capture, if the kernel is unchanged."""
+def _traffic(workload: str, partition_tokens: int):
+    """DRAM bytes per decode launch from a committed ncu capture, if the kernel and
+    the partition length are those of the capture."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -67,6 +68,8 @@ def _traffic(workload: str):
         return None
     src = os.path.join(ROOT, "paged_kv_cache_305_gb300", "csrc", "decode.cu")
     if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("source_sha256"):
+        return None
+    if rec.get("partition_tokens") != partition_tokens:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -486,12 +489,13 @@ def run_ours(args, rank, world, local_rank):
     dec_mean_ms = statistics.mean(dec_ms)
     achieved = kern_bytes / (dec_mean_ms * 1e-3) / 1e9
     value = job_throughput(step_bytes * K, world, ms) / 1e9
+    cfg = _config(case, args)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": W_steps, "ms_per_step": round(ms / K, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": case.dtype,
         "data": "synthetic",
-        "config": _config(case, args),
+        "config": cfg,
         "step_impl": "pa_decode_append (one kernel)" if fused else
                      "pa_reshape_and_cache + pa_decode" +
                      ("" if fused_ok or args.step != "fused" else
@@ -505,7 +509,7 @@ def run_ours(args, rank, world, local_rank):
         "roofline": {"kernel": "paged_decode_kernel" + (" (cache write fused)" if fused else ""),
                      "bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peak, "peak_kind": f"{peak_kind} hbm_gbs (copy)", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
+                     "frac": round(achieved / peak, 4), "traffic": _traffic(case.name, cfg["partition_tokens"]),
                      "algorithmic_bytes": kern_bytes,
                      "mean_launch_us": round(dec_mean_ms * 1e3, 2),
                      "median_launch_us": round(statistics.median(dec_ms) * 1e3, 2),
