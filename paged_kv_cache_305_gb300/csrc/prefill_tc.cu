@@ -444,6 +444,13 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     // value rows that the conversion pass wrote, block blk of sequence s at
     // block s * max_blocks_per_seq + blk (rejected block ids there are zeros)
     const bool from_v16 = SINGLE && Ty::kIsBf16 && is_v;
+    if (from_v16) {
+      // the copy is written by the conversion grid just before this one,
+      // which may still be running (programmatic dependent launch): wait for
+      // it to finish, then order its writes before this warp's TMA reads
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
     const T* cache = static_cast<const T*>(from_v16 ? a.v16 : (is_v ? a.value_cache : a.key_cache));
     const CUtensorMap* map = is_v ? &vmap : &kmap;
     const int full0 = is_v ? kBarVFull : kBarKFull;
@@ -688,6 +695,10 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
 // counts it). Values beyond fp16's range become +-inf.
 template <int D>
 __global__ void __launch_bounds__(256) v16_convert_kernel(const PrefillArgs a) {
+  // the prefill launched after this kernel may start its CTAs once every CTA
+  // here has started (programmatic dependent launch); only its V producer
+  // waits for this grid to finish
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j = blockIdx.x, s = blockIdx.y;
   const int shift = a.block_shift;
   const int B = 1 << shift;
@@ -757,15 +768,26 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, bool bf16, long long 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// after_convert: launched right behind the conversion pass as a programmatic
+// dependent launch (its CTAs may start while the pass is finishing).
 template <typename Ty, int D, bool SINGLE>
 cudaError_t launch_kernel(const CUtensorMap& km, const CUtensorMap& vm, const PrefillArgs& a,
-                          int tiles, cudaStream_t stream) {
+                          int tiles, bool after_convert, cudaStream_t stream) {
   auto kern = paged_prefill_tc_kernel<Ty, D, SINGLE>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, TcGeo<D>::kSmem);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(tiles, a.num_kv_heads, a.num_seqs), kThreads, TcGeo<D>::kSmem, stream>>>(km, vm, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles, a.num_kv_heads, a.num_seqs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = TcGeo<D>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_convert ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, km, vm, a);
 }
 
 template <typename Ty, int D>
@@ -787,11 +809,11 @@ cudaError_t launch_tc(const PrefillArgs& a, int max_query_len, cudaStream_t stre
     v16_convert_kernel<D><<<dim3(a.max_blocks_per_seq, a.num_seqs), 256, 0, stream>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    return launch_kernel<Ty, D, true>(km, vm, a, tiles, stream);
+    return launch_kernel<Ty, D, true>(km, vm, a, tiles, true, stream);
   }
   if (!encode_cache_map(&vm, a.value_cache, Ty::kIsBf16, slots, a.num_kv_heads, D, B))
     return cudaErrorInvalidValue;
-  return launch_kernel<Ty, D, !Ty::kIsBf16>(km, vm, a, tiles, stream);
+  return launch_kernel<Ty, D, !Ty::kIsBf16>(km, vm, a, tiles, false, stream);
 }
 
 }  // namespace
