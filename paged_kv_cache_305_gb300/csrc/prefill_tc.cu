@@ -8,7 +8,7 @@
 // One CTA per (query tile, kv head, sequence). A query tile is 128 rows =
 // 128 / G positions x the G heads of the kv head (the product's M), so each
 // K/V tile serves every query head of the group. Key tiles are 64 tokens.
-// Roles (7 warps):
+// Roles (8 warps):
 //   warps 0-3  one thread per query row: loads the query tile, then for every
 //              key tile reads its row of S = q K^T from tensor memory (and at
 //              once frees the S columns for the next tile's product), applies
@@ -26,11 +26,11 @@
 //              table), partial / out-of-range blocks by plain loads
 //              with zero fill; blocks under 8 tokens row by row with 16-byte
 //              cp.async; two stages, a K stage reused as soon as its S is done.
-//   warp 6     one thread issues the products: S_{j+1} = Q K_{j+1}^T (smem x
-//              smem, M=128, N=64) as soon as the softmax has read S_j, and
-//              O += P_j V_j (weights from tensor memory, V from smem read
-//              MN-major, N = head dim): one product for fp16, the head and
-//              the remainder for bf16.
+//   warp 6     one thread issues S_{j+1} = Q K_{j+1}^T (smem x smem, M=128,
+//              N=64) as soon as the softmax has read S_j;
+//   warp 7     one thread issues O += P_j V_j (weights from tensor memory, V
+//              from smem read MN-major, N = head dim): one product for fp16,
+//              the head and the remainder for bf16.
 // Tensor memory (256 columns): S at 0, P at 64, O at 128, so the product of
 // the next S overlaps the whole softmax of the current tile. All waits are
 // bounded; a wait that gives up is counted and the CTA winds down.
@@ -53,10 +53,11 @@ namespace {
 constexpr int kRows = 128;  // query rows per CTA = product M
 constexpr int kKeys = 64;   // tokens per key tile = N of S
 constexpr int kStages = 2;
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr int kKWarp = 4;    // producer of K tiles
 constexpr int kVWarp = 5;    // producer of V tiles
-constexpr int kMmaWarp = 6;  // one thread issues the products
+constexpr int kMmaWarp = 6;  // one thread issues the S products
+constexpr int kPvWarp = 7;   // one thread issues the P V products
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS = 0;    // S, 64 fp32 columns
 constexpr uint32_t kColP = 64;   // P: 32 columns of packed 16-bit heads, 32 of remainders
@@ -602,9 +603,11 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     for (int jj = max(0, j - kStages); jj < j; ++jj)
       tc::mbar_wait(bar(full0 + (jj & 1)), (jj >> 1) & 1);
     }
-  } else if (warp == kMmaWarp && lane == 0) {
-    // ---------------- products, one thread; descriptors built once, moved by
-    // adding (byte offset >> 4) to the start-address field
+  } else if ((warp == kMmaWarp || warp == kPvWarp) && lane == 0) {
+    // ---------------- products: S_j by one thread (warp kMmaWarp), P_j V by
+    // another (warp kPvWarp), so the next S never queues behind the issue of
+    // a P V; descriptors built once, moved by adding (byte offset >> 4) to
+    // the start-address field. Each thread's commits track its own products.
     const uint32_t id_s = tc::idesc_f16(kRows, kKeys, Ty::kIsBf16, false);
     // P V: fp16 weights with fp16 V, or bf16 weight parts with bf16 V
     const uint32_t id_o = tc::idesc_f16(kRows, D, SINGLE ? false : Ty::kIsBf16, true);
@@ -619,59 +622,53 @@ paged_prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
     auto kstep = [](int ks) {  // K-major: slice ks / 4, 32 bytes per 16 elements
       return static_cast<uint64_t>(((ks >> 2) * 1024 + (ks & 3) * 32) >> 4);
     };
-    auto issue_s = [&](int j) {
-      const int st = j & 1;
-      const uint32_t d = tmem + kColS;
-      const uint64_t dk = dk0 + st * kStageStep;
-#pragma unroll
-      for (int ks = 0; ks < kKSteps; ++ks) {
-        const uint64_t qoff = static_cast<uint64_t>(((ks >> 2) * Geo::kQHalf + (ks & 3) * 32) >> 4);
-        tc::mma_ss(d, dq0 + qoff, dk + kstep(ks), id_s, ks > 0 ? 1u : 0u);
-      }
-      tc::tc_commit(bar(kBarSFull + st));
-    };
-    uint32_t last_bar = 0, last_parity = 0;  // the latest commit
+    uint32_t last_bar = 0, last_parity = 0;  // this thread's latest commit
     // a stalled test launch first waits on a barrier that nothing signals:
     // the wait runs out, no product is issued, and every warp winds down
     if (a.stall_for_test) ok = tc::mbar_wait(bar(kBarNever), 0);
-    ok = ok && tc::mbar_wait(bar(kBarQFull), 0) && tc::mbar_wait(bar(kBarKFull), 0);
-    if (ok) {
-      tc::tc_fence_after();
-      if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products
-      issue_s(0);
-      last_bar = bar(kBarSFull);
-      last_parity = 0;
-    }
-    for (int j = 0; j < ntiles && ok; ++j) {
-      const int b = j & 1;
-      if (j + 1 < ntiles) {
-        // S_{j+1} overwrites S_j: wait until the softmax has read it
-        ok = tc::mbar_wait(bar(kBarSFree), j & 1) &&
-             tc::mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1);
+    if (warp == kMmaWarp) {
+      for (int j = 0; j < ntiles && ok; ++j) {
+        // S_j overwrites S_{j-1}: wait until the softmax has read it
+        ok = (j == 0 ? tc::mbar_wait(bar(kBarQFull), 0)
+                     : tc::mbar_wait(bar(kBarSFree), (j - 1) & 1)) &&
+             tc::mbar_wait(bar(kBarKFull + (j & 1)), (j >> 1) & 1);
+        if (!ok) break;
+        tc::tc_fence_after();
+        if (row_copies) tc::fence_async_smem();  // rows written by cp.async, seen by the products
+        const int st = j & 1;
+        const uint64_t dk = dk0 + st * kStageStep;
+#pragma unroll
+        for (int ks = 0; ks < kKSteps; ++ks) {
+          const uint64_t qoff =
+              static_cast<uint64_t>(((ks >> 2) * Geo::kQHalf + (ks & 3) * 32) >> 4);
+          tc::mma_ss(tmem + kColS, dq0 + qoff, dk + kstep(ks), id_s, ks > 0 ? 1u : 0u);
+        }
+        tc::tc_commit(bar(kBarSFull + st));
+        last_bar = bar(kBarSFull + st);
+        last_parity = (j >> 1) & 1;
+      }
+    } else {
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int b = j & 1;
+        ok = tc::mbar_wait(bar(kBarPFull), j & 1) &&
+             tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
         if (!ok) break;
         tc::tc_fence_after();
         if (row_copies) tc::fence_async_smem();
-        issue_s(j + 1);
-        last_bar = bar(kBarSFull + ((j + 1) & 1));
-        last_parity = ((j + 1) >> 1) & 1;
-      }
-      ok = tc::mbar_wait(bar(kBarPFull), j & 1) && tc::mbar_wait(bar(kBarVFull + b), (j >> 1) & 1);
-      if (!ok) break;
-      tc::tc_fence_after();
-      if (row_copies) tc::fence_async_smem();
-      const uint32_t colP = tmem + kColP;
-      const uint64_t dv = dv0 + b * kStageStep;
-      // fp16: one product; bf16: the weights' head part, then the remainder
+        const uint32_t colP = tmem + kColP;
+        const uint64_t dv = dv0 + b * kStageStep;
+        // fp16: one product; bf16: the weights' head part, then the remainder
 #pragma unroll
-      for (int part = 0; part < (SINGLE ? 1 : 2); ++part) {
+        for (int part = 0; part < (SINGLE ? 1 : 2); ++part) {
 #pragma unroll
-        for (int ks = 0; ks < kKeys / 16; ++ks)
-          tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
-                     id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kKeys / 16; ++ks)
+            tc::mma_ts(tmem + kColO, colP + part * 32 + ks * 8, dv + ks * kVStep,
+                       id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+        }
+        tc::tc_commit(bar(kBarODone + b));
+        last_bar = bar(kBarODone + b);
+        last_parity = (j >> 1) & 1;
       }
-      tc::tc_commit(bar(kBarODone + b));
-      last_bar = bar(kBarODone + b);
-      last_parity = (j >> 1) & 1;
     }
     // nothing this thread issued may still be running when the CTA ends
     if (last_bar != 0) tc::mbar_wait(last_bar, last_parity);
