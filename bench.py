@@ -753,8 +753,14 @@ def measure_prefill(ctx, chunk, B, tname, steps, warmup, S=16, Hq=32, Hkv=8, d=1
     # bf16: with the workspace the call converts the value rows to fp16 first
     # (a second kernel, timed with it) and P.V is one product
     ws = pa.alloc_prefill_workspace(sl, kc, bt) if workspace else None
+    pa.wait_timeout_count(clear=True)
     ms = _events(lambda: pa.prefill(out, q, kc, vc, bt, sl, starts, chunk, case.scale, ws),
                  steps, max(3, warmup))
+    # a bounded in-kernel wait that gave up means a CTA wound down early: the
+    # timing would not be of the whole computation
+    timeouts = pa.wait_timeout_count(clear=True)
+    if timeouts:
+        raise RuntimeError(f"prefill: {timeouts} bounded waits gave up during the measurement")
     pairs = S * sum(ctx - chunk + j + 1 for j in range(chunk))
     tf = 4.0 * d * Hq * pairs / (ms * 1e-3) / 1e12
     peak, kind = _bf16_peak()
