@@ -9,8 +9,6 @@ limit one token too short or too long, positions counted from the chunk start.
 With any one of them in place, at least one pin of ``test_oracle.py`` /
 ``test_oracle_prefill.py`` must fail; with none, all of them pass.
 """
-import math
-
 import numpy as np
 import pytest
 
