@@ -57,6 +57,14 @@ def _peaks():
     return 6800.0, "fallback"
 
 
+def _decode_source_sha() -> str:
+    """SHA-256 over the decode kernel's source and the header of its constants."""
+    h = hashlib.sha256()
+    for name in ("decode.cu", "internal.h"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_305_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def _traffic(workload: str, partition_tokens: int):
     """DRAM bytes per decode launch from a committed ncu capture, if the kernel and
     the partition length are those of the capture."""
@@ -66,8 +74,7 @@ def _traffic(workload: str, partition_tokens: int):
     rec = json.load(open(p)).get(workload)
     if not rec:
         return None
-    src = os.path.join(ROOT, "paged_kv_cache_305_gb300", "csrc", "decode.cu")
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() != rec.get("source_sha256"):
+    if _decode_source_sha() != rec.get("source_sha256"):
         return None
     if rec.get("partition_tokens") != partition_tokens:
         return None

@@ -99,7 +99,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_q_heads, int head_dim, in
 
 // Scheduling of the persistent decode kernel: a partition weighs its tokens
 // plus kUnitCost; a CTA keeps at most kMaxSegments segment records at a time.
-constexpr int kUnitCost = 32;
+constexpr int kUnitCost = 64;
 constexpr int kMaxSegments = 64;
 
 // Launchers: return a cudaError_t from the launch (cudaSuccess on success).
